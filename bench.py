@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of paged MLA decode over a quantized latent KV cache (FP8 E4M3 / NVFP4) on GB300.
+
+Prints one JSON line. The headline metric is the KV bytes read per second by one decode step (one
+layer) of the FP8 workload of 44 requests x 32,768 tokens, 128 heads (``mla_fp8_b44_h128_l32k``),
+with its microseconds per step and its fraction of the measured HBM peak. The same line carries the
+NVFP4 workloads (10 x 163,840 tokens with a per-step append; 1 x 1,048,576 tokens, global scale 1 and
+calibrated) and the mixed serving batch against the cast-then-attend baseline, each timed the same way.
+
+Timing: CUDA events on the launching stream around exactly --steps steps after --warmup untimed
+steps, with a barrier and a device synchronisation on both sides; every workload reads more KV per
+step than the 129 MB L2 holds, so no flush is needed. The decode kernel is also timed alone
+(events around each of its launches) for the roofline. `e2e` repeats the headline through the
+public API with host buffers: per step the host plan, the table and Q uploads, the decode and the
+read-back of the output and lse. `cpu_baseline` times the FP64 CPU oracle on a bounded sample.
+
+--impl reference runs the oracle alone on the host cores, on the same workload and metric.
+With --gpus N (launched under torch.distributed.run) every rank runs its own replica: the path has
+no exchange step, so there is no collective on the data path; value = bytes of all ranks / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+MAIN = "mla_fp8_b44_h128_l32k"
+LATENT, DV = 576, 512
+FLOPS_PER_TOKEN_HEAD = 2 * (LATENT + DV)        # Q.K^T over 576 dims + P.V over 512 dims
+METRIC = "MLA decode KV read bandwidth (FP8 E4M3 latent cache, 44 x 32K tokens, 128 heads)"
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        p.update({k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in d})
+        p["source"] = "measured"
+    return p
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_kv_paged_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = kernel_source_digest()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == workload and parts[1] == digest:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def calibrated_scale(w):
+    amax = float(w.src_fp8.view(torch.float8_e4m3fn).float().abs().max())
+    return float(np.float32(amax) / np.float32(2688.0))
+
+
+class Problem:
+    """A workload resident on the GPU with its plan, workspace and outputs."""
+
+    def __init__(self, q, w, kv, g=1.0, min_splits=0, algo=0, append=False, bf16_pool=False):
+        self.q, self.w, self.kv, self.g, self.append = q, w, kv, g, append
+        dev = w.pool_fp8.device
+        self.dev = dev
+        if kv == q.KV_NVFP4:
+            self.data = torch.full((w.num_pages, 64, 288), 0xFF, dtype=torch.uint8, device=dev)
+            self.scale = torch.full((w.num_pages, 64, 36), 0x7F, dtype=torch.uint8, device=dev)
+            q.kv_append_quant(w.src_fp8, q.SRC_FP8_E4M3, w.slots, self.data, self.scale, q.KV_NVFP4, g)
+        elif kv == q.KV_BF16:
+            self.data = torch.empty((w.num_pages, 64, LATENT), dtype=torch.int16, device=dev)
+            self.scale = None
+        else:
+            self.data, self.scale = w.pool_fp8, None
+        self.lens = w.kv_len.copy()
+        if append:
+            self.app_src, self.app_slots = synth.append_tokens(w, dev)
+            self.lens = self.lens + 1
+        self.min_splits, self.algo = min_splits, algo
+        p = q.mla_decode_plan(w.kv_indptr, self.lens, w.heads, kv, min_splits=min_splits, algo=algo)
+        self.ws = torch.empty(max(256, p.workspace_bytes), dtype=torch.uint8, device=dev)
+        self.plan = q.mla_decode_plan(w.kv_indptr, self.lens, w.heads, kv, min_splits=min_splits,
+                                      algo=algo, workspace=self.ws)
+        self.idx = torch.from_numpy(w.kv_indices).to(dev)
+        self.out = torch.empty((w.batch, w.heads, DV), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.batch, w.heads), dtype=torch.float32, device=dev)
+        self.tokens = int(self.lens.sum())
+        bpt = {q.KV_FP8_E4M3: LATENT, q.KV_NVFP4: 324, q.KV_BF16: 2 * LATENT}[kv]
+        self.kv_bytes = self.tokens * bpt
+        self.flops = self.tokens * w.heads * FLOPS_PER_TOKEN_HEAD
+        self.needs_combine = self.plan.num_split_requests > 0 or self.plan.num_empty_requests > 0
+
+    def launches_per_step(self):
+        return (1 if self.append else 0) + 1 + (1 if self.needs_combine else 0)
+
+    def step(self, ev_a=None, ev_b=None):
+        q, w = self.q, self.w
+        if self.append:
+            q.kv_append_quant(self.app_src, q.SRC_FP8_E4M3, self.app_slots, self.data, self.scale, self.kv, self.g)
+        if ev_a is not None:
+            ev_a.record()
+        q.mla_decode_attend(self.plan, w.q, self.data, self.scale, w.num_pages, self.idx, w.sm_scale,
+                            self.g, self.out, self.lse, self.ws)
+        if ev_b is not None:
+            ev_b.record()
+        q.mla_decode_combine(self.plan, self.g, self.out, self.lse, self.ws)
+
+
+def time_problem(pb: Problem, steps: int, warmup: int, world: int = 1):
+    for _ in range(warmup):
+        pb.step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record()
+    for k in range(steps):
+        pb.step(*ev[k])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = t0.elapsed_time(t1) / steps
+    attend_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    return ms, attend_ms
+
+
+def summarize(pb: Problem, ms: float, attend_ms: float, pk: dict):
+    s = ms * 1e-3
+    return {
+        "us_per_step": round(ms * 1e3, 2),
+        "decode_kernel_us": round(attend_ms * 1e3, 2),
+        "kv_bytes": pb.kv_bytes,
+        "kv_gbs": round(pb.kv_bytes / s / 1e9, 1),
+        "hbm_frac_of_measured": round(pb.kv_bytes / s / 1e9 / pk["hbm_gbs"], 4),
+        "tflops": round(pb.flops / s / 1e12, 1),
+        "tensor_frac_of_measured": round(pb.flops / s / 1e12 / pk["bf16_tflops"], 4),
+        "segments": pb.plan.num_segments,
+        "launches_per_step": pb.launches_per_step(),
+    }
+
+
+def e2e_main(q, pb: Problem, steps: int, warmup: int):
+    """Headline through the public API with host buffers: host plan + H2D (table, Q) + decode +
+    D2H (out, lse) every step."""
+    w = pb.w
+    q_host = w.q.cpu().pin_memory()
+    out_host = torch.empty(pb.out.shape, dtype=pb.out.dtype).pin_memory()
+    lse_host = torch.empty(pb.lse.shape, dtype=pb.lse.dtype).pin_memory()
+    q_dev = torch.empty_like(w.q)
+
+    def one():
+        plan = q.mla_decode_plan(w.kv_indptr, pb.lens, w.heads, pb.kv, min_splits=pb.min_splits,
+                                 algo=pb.algo, workspace=pb.ws)
+        q_dev.copy_(q_host, non_blocking=True)
+        q.mla_decode_run(plan, q_dev, pb.data, pb.scale, w.num_pages, pb.idx, w.sm_scale, pb.g,
+                         pb.out, pb.lse, pb.ws)
+        out_host.copy_(pb.out, non_blocking=True)
+        lse_host.copy_(pb.lse, non_blocking=True)
+        return plan
+
+    for _ in range(warmup):
+        plan = one()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    s = (time.perf_counter() - t) / steps
+    h2d = q_host.numel() * 2 + plan.table_bytes
+    d2h = out_host.numel() * 2 + lse_host.numel() * 4
+    return {"value": round(pb.kv_bytes / s / 1e9, 1), "unit": "GB/s", "us_per_step": round(s * 1e6, 1),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def oracle_sample(w, host_pool, kv=1, g=1.0, budget_s=15.0, lens=None):
+    """Time the FP64 oracle on whole requests (all heads) of the workload until ~budget_s."""
+    import oracle
+    qb = w.q.cpu().view(torch.int16).numpy().view(np.uint16)
+    lens = w.kv_len if lens is None else lens
+    n_threads = oracle.threads()
+    done_pairs, t_total = 0, 0.0
+    H = w.heads
+    r = 0
+    while t_total < budget_s and r < w.batch:
+        pairs = np.array([[r, h] for h in range(H)], np.int32)
+        t = time.perf_counter()
+        oracle.mla_decode(qb, host_pool[0], host_pool[1], kv, 64, w.num_pages, w.kv_indptr, w.kv_indices,
+                          lens, w.sm_scale, g, pairs)
+        t_total += time.perf_counter() - t
+        done_pairs += H
+        r += 1
+    req = done_pairs / H
+    bytes_ = sum(int(lens[i]) for i in range(r)) * LATENT
+    return {"value": round(bytes_ / t_total / 1e9, 4), "unit": "GB/s", "cores": n_threads, "kind": "oracle",
+            "sample": f"{int(req)} of {w.batch} requests x {H} heads of {w.name} ({t_total:.1f} s)",
+            "us_per_step_equivalent": round(t_total / req * w.batch * 1e6, 1)}
+
+
+def run_reference(args):
+    """The reference arm: the FP64 CPU oracle as it stands, on the headline workload."""
+    import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = synth.workload(MAIN, device=dev)
+    host = (w.pool_fp8.cpu().numpy(), None)
+    qb = w.q.cpu().view(torch.int16).numpy().view(np.uint16)
+    H = w.heads
+    # size each step so warmup + steps take about two minutes in all
+    t = time.perf_counter()
+    oracle.mla_decode(qb, host[0], None, 1, 64, w.num_pages, w.kv_indptr, w.kv_indices, w.kv_len,
+                      w.sm_scale, 1.0, np.array([[0, 0]], np.int32), nthreads=1)
+    per_pair_1t = time.perf_counter() - t
+    threads = oracle.threads()
+    per_pair = per_pair_1t / max(1, threads)
+    budget = 120.0 / (args.steps + args.warmup)
+    n_pairs = int(max(1, min(H * w.batch, budget / per_pair)))
+    pairs_all = np.array([[r, h] for r in range(w.batch) for h in range(H)], np.int32)
+    times = []
+    for k in range(args.warmup + args.steps):
+        sel = pairs_all[(k * n_pairs + np.arange(n_pairs)) % len(pairs_all)]
+        t = time.perf_counter()
+        oracle.mla_decode(qb, host[0], None, 1, 64, w.num_pages, w.kv_indptr, w.kv_indices, w.kv_len,
+                          w.sm_scale, 1.0, sel)
+        if k >= args.warmup:
+            times.append(time.perf_counter() - t)
+    s = float(np.sum(times)) / args.steps
+    L = int(w.kv_len[0])
+    bytes_per_step = n_pairs / H * L * LATENT
+    value = round(bytes_per_step / s / 1e9, 4)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded SplitMix64 normals, FP8 E4M3 latent with 4 outlier channels x20)",
+            "config": {"workload": MAIN, "batch": w.batch, "heads": H, "context": L, "kv_dtype": "fp8_e4m3",
+                       "page_size": 64, "sample_pairs_per_step": n_pairs},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_pairs} (request, head) pairs of {MAIN} per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--algo", type=int, default=0)
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--out", default=None, help="also write the JSON line to this file")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import quantized_kv_paged_gb300 as q
+    q.load()
+    pk = peaks()
+    dev = torch.device("cuda", local)
+
+    # ---- headline: FP8, 44 x 32K, 128 heads ----
+    w = synth.workload(MAIN, device=dev)
+    pb = Problem(q, w, q.KV_FP8_E4M3, algo=args.algo)
+    with ClockSampler(local) as clk:
+        ms, attend_ms = time_problem(pb, args.steps, args.warmup, world)
+    ms_max = max_over_ranks(ms, world, dev)
+    value = world * pb.kv_bytes / (ms_max * 1e-3) / 1e9
+    main_stats = summarize(pb, ms, attend_ms, pk)
+    attend_s = attend_ms * 1e-3
+    roof = {"bound": "tensor", "kernel": "decode_mma_kernel (split-KV attend)",
+            "achieved": round(pb.flops / attend_s / 1e12, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(pb.flops / attend_s / 1e12 / pk["bf16_tflops"], 4),
+            "traffic": profiled_traffic(MAIN),
+            "peak_note": f"{pk['source']} BF16 dense burst; FP16 operands run at the BF16 rate",
+            "hbm": {"achieved": round(pb.kv_bytes / attend_s / 1e9, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(pb.kv_bytes / attend_s / 1e9 / pk["hbm_gbs"], 4)},
+            "algorithmic_bytes_per_launch": pb.kv_bytes, "algorithmic_flops_per_launch": pb.flops}
+    e2e = e2e_main(q, pb, min(args.steps, 50), 3)
+    gpu_launches = args.steps * pb.launches_per_step()
+    extra = {}
+    if rank == 0 and world == 1 and not args.no_extra:
+        extra = extra_workloads(q, pk, dev, args, host_main=None)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = oracle_sample(w, (w.pool_fp8.cpu().numpy(), None))
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "us_per_step": round(ms_max * 1e3, 2),
+        "hbm_frac_of_measured": round(value / world / pk["hbm_gbs"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded SplitMix64 normals, FP8 E4M3 latent with 4 outlier channels x20, BF16 Q)",
+        "config": {"workload": MAIN, "batch": w.batch, "heads": w.heads, "context": int(w.kv_len[0]),
+                   "kv_dtype": "fp8_e4m3", "page_size": 64, "pool_tokens": w.num_pages * 64,
+                   "algo": "mma_sync" if pb.plan.algo == 1 else "tcgen05",
+                   "l2": f"inputs larger than L2 ({pb.kv_bytes / 1e6:.0f} MB of KV read per step)"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clk.summary(),
+        "cpu_baseline": cpu, "main": main_stats, "workloads": extra,
+        "kernel_digest": kernel_source_digest(),
+    }
+    if rank == 0:
+        s = json.dumps(line)
+        print(s, flush=True)
+        if args.out:
+            with open(args.out, "w") as f:
+                f.write(s + "\n")
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def extra_workloads(q, pk, dev, args, host_main=None):
+    steps = max(10, min(args.steps, 50))
+    res = {}
+    # NVFP4, 10 x 163,840 (+1 appended per step), 128 heads
+    w = synth.workload("mla_nvfp4_b10_h128_l160k", device=dev)
+    pb = Problem(q, w, q.KV_NVFP4, g=1.0, append=True, algo=args.algo)
+    ms, att = time_problem(pb, steps, args.warmup)
+    res["mla_nvfp4_b10_h128_l160k"] = summarize(pb, ms, att, pk)
+    del pb, w
+    torch.cuda.empty_cache()
+    # NVFP4, 1 x 1,048,576, >= 148 splits, global scale 1 and calibrated
+    w = synth.workload("mla_nvfp4_b1_h128_l1m", device=dev)
+    for tag, g in (("g1", 1.0), ("calibrated", calibrated_scale(w))):
+        pb = Problem(q, w, q.KV_NVFP4, g=g, min_splits=148, algo=args.algo)
+        ms, att = time_problem(pb, steps, args.warmup)
+        r = summarize(pb, ms, att, pk)
+        r["global_scale"] = g
+        res[f"mla_nvfp4_b1_h128_l1m_{tag}"] = r
+        del pb
+    del w
+    torch.cuda.empty_cache()
+    # mixed serving batch: fused FP8 decode vs cast-then-attend (pool cast to BF16 + BF16 decode)
+    w = synth.workload("mla_fp8_mixed_b64_h128_pool495552", device=dev)
+    fused = Problem(q, w, q.KV_FP8_E4M3, algo=args.algo)
+    ms, att = time_problem(fused, steps, args.warmup)
+    r = summarize(fused, ms, att, pk)
+    base = Problem(q, w, q.KV_BF16, algo=args.algo)
+    cast_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for _ in range(args.warmup):
+        q.kv_pool_cast_bf16(w.pool_fp8, base.data)
+        base.step()
+    torch.cuda.synchronize()
+    for k in range(steps):
+        cast_ev[k][0].record()
+        q.kv_pool_cast_bf16(w.pool_fp8, base.data)
+        cast_ev[k][1].record()
+        dec_ev[k][0].record()
+        base.step()
+        dec_ev[k][1].record()
+    torch.cuda.synchronize()
+    cast_ms = float(np.mean([a.elapsed_time(b) for a, b in cast_ev]))
+    bdec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
+    pool_bytes = w.num_pages * 64 * LATENT
+    r["cast_then_attend"] = {
+        "cast_us": round(cast_ms * 1e3, 2), "cast_bytes": 3 * pool_bytes,
+        "cast_gbs": round(3 * pool_bytes / (cast_ms * 1e-3) / 1e9, 1),
+        "bf16_decode_us": round(bdec_ms * 1e3, 2),
+        "us_per_layer": round((cast_ms + bdec_ms) * 1e3, 2),
+        "ms_per_78_layers": round(78 * (cast_ms + bdec_ms), 3)}
+    r["fused_ms_per_78_layers"] = round(78 * ms, 3)
+    r["speedup_vs_cast_then_attend"] = round((cast_ms + bdec_ms) / ms, 2)
+    res["mla_fp8_mixed_b64_h128_pool495552"] = r
+    return res
+
+
+if __name__ == "__main__":
+    main()

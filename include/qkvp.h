@@ -1,0 +1,227 @@
+/*
+ * qkvp.h - C ABI of libqkvp: paged MLA decode attention that reads a quantized latent KV cache
+ * (FP8 E4M3 or NVFP4) directly, for NVIDIA GB300 (sm_103a).
+ *
+ * The problem, as the source pages state it:
+ *  - Each token stores one 576-wide latent: kv_lora_rank 512 ("nope") + qk_rope_head_dim 64. All
+ *    query heads share it. Attention uses K = the whole latent and V = its first 512 dims ("The
+ *    Smoking Gun: Tracing the FP8-to-BF16 KV Cache Cast", section "The Investigation Leading to This
+ *    Message": pool shape [495552, 1, 576]).
+ *  - The pool is paged and addressed through a CSR page table (qo_indptr, kv_indptr, kv_indices,
+ *    kv_len_arr), with num_heads, kv_lora_rank, qk_rope_head_dim, page_size, sm_scale and the KV
+ *    dtype given to a host-side plan() before a device-side run() ("The Smoking Gun", section
+ *    "What Message 1408 Actually Reveals").
+ *  - The KV cache is FP8 E4M3 (float8_e4m3fn; "The FP8 KV Cache Wall", section "Context and
+ *    Motivation") or NVFP4: E2M1 values, one E4M3 scale per 16 values, one FP32 global scale per
+ *    tensor ("SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "NVFP4 format").
+ *  - Decode reads the quantized pages directly and dequantizes inside the kernel; nothing casts the
+ *    pool to BF16 first (same page, section "SGLang implementation", item 3).
+ *
+ * Memory layout (all device buffers are caller-owned; the library allocates no device memory and
+ * keeps no global mutable state):
+ *  - slot s = page * page_size + offset; page_size must be 64.
+ *  - FP8 pool  : kv_data uint8 [num_pages][64][576], one E4M3 byte per latent element.
+ *  - NVFP4 pool: kv_data uint8 [num_pages][64][288] packed E2M1 pairs (element 2k in the low nibble
+ *                of byte k, 2k+1 in the high nibble) and kv_scale uint8 [num_pages][64][36] E4M3
+ *                block scales (block j covers elements 16j..16j+15). 324 bytes per token = 9/16 of
+ *                FP8. An element decodes to global_scale * scale(block) * e2m1(code).
+ *  - BF16 pool : kv_data uint16 [num_pages][64][576] (the cast-then-attend baseline only).
+ *  - q         : bf16 [batch][num_heads][576], row-major, contiguous.
+ *  - out       : bf16 [batch][num_heads][512]; lse: float [batch][num_heads] (natural log), or NULL.
+ *
+ * Errors: every call returns an int status (qkvp_status). Arguments are checked before anything is
+ * launched; a failed check launches nothing. QKVP_E_CUDA reports a CUDA error from a launch or copy
+ * issued by the call. Faults that occur asynchronously inside a kernel surface at the caller's next
+ * synchronisation. Indices read from device memory (slot ids, page ids) are bounds-checked in the
+ * kernels: out-of-range entries are skipped (append) or read as masked tokens (decode); they never
+ * cause an out-of-bounds access.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are asynchronous
+ * with respect to the host unless stated. The library is re-entrant across distinct streams and
+ * workspaces.
+ */
+#ifndef QKVP_H_
+#define QKVP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qkvp_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  QKVP_OK = 0,
+  QKVP_E_INVALID = -1,     /* bad argument: null pointer, negative size, inconsistent page table */
+  QKVP_E_UNSUPPORTED = -2, /* valid but not supported: page size, head count, dtype combination */
+  QKVP_E_WORKSPACE = -3,   /* workspace missing or smaller than plan->workspace_bytes */
+  QKVP_E_CUDA = -4         /* a CUDA runtime call or launch failed */
+} qkvp_status;
+
+typedef enum { QKVP_KV_FP8_E4M3 = 1, QKVP_KV_NVFP4 = 2, QKVP_KV_BF16 = 3 } qkvp_kv_dtype;
+typedef enum { QKVP_SRC_FP8_E4M3 = 1, QKVP_SRC_BF16 = 2 } qkvp_src_dtype;
+
+/* Decode kernel families. AUTO lets the planner choose. */
+typedef enum {
+  QKVP_ALGO_AUTO = 0,
+  QKVP_ALGO_MMA_SYNC = 1,  /* warp-level mma.sync BF16 split-KV kernel */
+  QKVP_ALGO_TCGEN05 = 2    /* tcgen05/TMEM CTA-pair split-KV kernel */
+} qkvp_algo;
+
+#define QKVP_LATENT_DIM 576
+#define QKVP_V_DIM 512
+#define QKVP_PAGE_SIZE 64
+
+/* Host-side plan produced by mla_decode_plan and consumed by mla_decode_run. Plain data: it may be
+ * copied, and one plan serves any number of runs (e.g. one per layer) with the same page table,
+ * lengths, head count and KV dtype, as long as the workspace it was uploaded to is left intact. */
+typedef struct {
+  int32_t batch, num_heads, page_size, kv_dtype;
+  int32_t algo;              /* the kernel family the plan was made for */
+  int32_t num_workers;       /* independent split-KV workers (one CTA pair or CTA group each) */
+  int32_t ctas_per_worker;   /* CTAs that cooperate on one worker's token ranges */
+  int32_t num_segments;      /* (request, page range) pieces; each writes one partial or output */
+  int32_t num_split_requests;/* requests whose pages span more than one segment (need a combine) */
+  int32_t num_empty_requests;/* requests with no tokens (output 0, lse -inf) */
+  int32_t max_worker_pages;  /* most pages given to one worker (load balance) */
+  int32_t min_worker_pages;  /* fewest pages given to one worker */
+  int32_t num_partials;      /* FP32 split partials held in the workspace */
+  int64_t total_pages;       /* sum over requests of ceil(len / 64) */
+  int64_t total_tokens;      /* sum of lengths */
+  uint64_t workspace_bytes;  /* device workspace the run needs (table + split partials) */
+  uint64_t table_bytes;      /* bytes of the work table at the start of the workspace */
+  uint64_t partial_o_offset; /* byte offset of the FP32 partial outputs in the workspace */
+  uint64_t partial_lse_offset;
+  uint64_t magic;            /* set by a successful plan; checked by run */
+} qkvp_plan;
+
+/*
+ * kv_append_quant - quantize-on-append: write n_tokens new latent rows into the paged pool.
+ *
+ * Source: "SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "SGLang implementation", items 1-2
+ * (quantize KV from FP8 into NVFP4 and write it to the persistent cache); section "NVFP4 format"
+ * (two-level scaling). For an FP8 pool: E4M3 storage of the latent ("The FP8 KV Cache Wall").
+ *
+ *  src          device, [n_tokens][576]: E4M3 bytes (src_dtype QKVP_SRC_FP8_E4M3) or BF16
+ *               (QKVP_SRC_BF16).
+ *  slot_mapping device int64 [n_tokens]: destination slot page * page_size + offset; a negative slot
+ *               skips the token; a slot >= num_pages * page_size is skipped too.
+ *  kv_data      device pool (layout above) for kv_dtype QKVP_KV_FP8_E4M3 or QKVP_KV_NVFP4.
+ *  kv_scale     device NVFP4 block-scale pool; must be NULL for FP8.
+ *  global_scale NVFP4 decode multiplier g (> 0, finite): an element decodes to g * s * e. Must be
+ *               1.0 for FP8.
+ *
+ * FP8 pool: FP8 sources are copied; BF16 sources round to nearest even, saturating at +-448; NaN
+ * gives 0x7F. NVFP4 pool, per block of 16 consecutive elements x (FP32 arithmetic, one rounding per
+ * operation): amax = max|x| (NaN if any x is NaN); s8 = E4M3(amax / (6 g)) rounded to nearest even
+ * and saturated; sd = value(s8) * g; codes = 0 where sd == 0, else E2M1(x / sd) rounded to nearest
+ * even and saturated at +-6 (NaN gives 0). The stored bytes are bit-identical to the CPU oracle.
+ * If two tokens of one call name the same slot, which of them is stored is unspecified.
+ */
+int kv_append_quant(const void* src, int32_t src_dtype, int64_t n_tokens,
+                    const int64_t* slot_mapping, void* kv_data, uint8_t* kv_scale,
+                    int32_t kv_dtype, float global_scale, int32_t page_size, int64_t num_pages,
+                    qkvp_stream_t stream);
+
+/*
+ * mla_decode_plan - split the batch's pages into balanced work for the decode kernel.
+ *
+ * Source: the plan/run split and CSR page table of the pages' plan() call ("The Smoking Gun",
+ * section "What Message 1408 Actually Reveals"). The split-KV decomposition itself is not on the
+ * pages; its partial results are merged by log-sum-exp in mla_decode_run.
+ *
+ *  kv_indptr_host host int32 [batch + 1], in pages: request r owns kv_indices[kv_indptr[r] ..
+ *                 kv_indptr[r+1]). Must start at 0 and be non-decreasing.
+ *  kv_len_host    host int32 [batch], tokens per request; ceil(len / 64) must not exceed the
+ *                 request's page count. len 0 is allowed (output 0, lse -inf).
+ *  num_heads      query heads: a multiple of 16 in [16, 128].
+ *  page_size      must be 64.
+ *  num_sms        streaming multiprocessors to plan for; <= 0 queries the current device (a CUDA
+ *                 runtime call, also in query mode).
+ *  min_splits     lower bound on the number of segments (e.g. 148 to spread one long request over
+ *                 every SM); 0 for none.
+ *  algo           a qkvp_algo; QKVP_ALGO_AUTO picks the fastest supported family.
+ *  workspace      device buffer that receives the work table; NULL makes this a pure host query
+ *                 that only fills *plan (including plan->workspace_bytes) and touches no device.
+ *  stream         stream of the table upload (an asynchronous copy from library-owned staging, so
+ *                 the host arrays may be reused as soon as this returns).
+ *
+ * Returns QKVP_E_WORKSPACE (with plan->workspace_bytes filled) when workspace is non-NULL but
+ * smaller than needed.
+ */
+int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int32_t batch,
+                    int32_t num_heads, int32_t page_size, int32_t kv_dtype, int32_t num_sms,
+                    int32_t min_splits, int32_t algo, void* workspace, uint64_t workspace_bytes,
+                    qkvp_stream_t stream, qkvp_plan* plan);
+
+/*
+ * mla_decode_run - paged MLA decode attention over the quantized pool, for one layer.
+ *
+ * Computes, per request r and head h over its tokens t < len_r (in natural-log terms),
+ *   z_t = sm_scale * g * sum_{d<576} q[r,h,d] * k_t[d]
+ *   out[r,h,v] = g * sum_t softmax(z)_t * k_t[v] (v < 512),   lse[r,h] = log sum_t exp(z_t)
+ * where k_t is the dequantized latent without the global scale g (g = 1 for FP8 and BF16 pools;
+ * "SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "SGLang implementation", item 3: the global
+ * scale enters through the matrix-multiply scaling, not per element). The kernels dequantize in
+ * registers, run Q.K^T and P.V on the tensor cores in BF16 with FP32 accumulation and an FP32
+ * online softmax, write one partial per segment, and merge partials by log-sum-exp.
+ *
+ *  plan       from mla_decode_plan with the same kv_dtype, uploaded into this workspace.
+ *  q          device bf16 [batch][num_heads][576].
+ *  kv_data    device pool for plan->kv_dtype; kv_scale the NVFP4 scale pool (NULL otherwise).
+ *  num_pages  pages in the pool; page ids outside [0, num_pages) read as masked tokens.
+ *  kv_indices device int32 page ids addressed by the plan's kv_indptr.
+ *  sm_scale   logit scale (finite); global_scale: NVFP4 g (> 0, finite), must be 1.0 otherwise.
+ *  out, lse   outputs (lse may be NULL).
+ *  workspace  the buffer given to mla_decode_plan, at least plan->workspace_bytes.
+ */
+int mla_decode_run(const qkvp_plan* plan, const void* q, const void* kv_data,
+                   const uint8_t* kv_scale, int64_t num_pages, const int32_t* kv_indices,
+                   float sm_scale, float global_scale, void* out, float* lse, void* workspace,
+                   uint64_t workspace_bytes, qkvp_stream_t stream);
+
+/*
+ * mla_decode_attend / mla_decode_combine - the two halves of mla_decode_run, for callers that
+ * schedule or time them separately. attend runs the split-KV decode kernel: requests covered by a
+ * single segment get their final out/lse, the others leave FP32 partials (normalised output and
+ * base-2 log-sum-exp) in the workspace. combine merges those partials by log-sum-exp into out/lse
+ * and writes zeros / -inf for empty requests. combine must follow attend on the same stream with
+ * the same plan, workspace, global_scale, out and lse. Arguments as for mla_decode_run.
+ */
+int mla_decode_attend(const qkvp_plan* plan, const void* q, const void* kv_data,
+                      const uint8_t* kv_scale, int64_t num_pages, const int32_t* kv_indices,
+                      float sm_scale, float global_scale, void* out, float* lse, void* workspace,
+                      uint64_t workspace_bytes, qkvp_stream_t stream);
+int mla_decode_combine(const qkvp_plan* plan, float global_scale, void* out, float* lse,
+                       void* workspace, uint64_t workspace_bytes, qkvp_stream_t stream);
+
+/*
+ * kv_pool_cast_bf16 - the cast-then-attend baseline's pool-wide cast: every E4M3 byte of an FP8
+ * pool to its BF16 value (exact; NaN bytes 0x7F/0xFF become 0x7FC0). Source: "The Smoking Gun",
+ * section "The Investigation Leading to This Message" (k_buffer = pool.to(q.dtype) over the whole
+ * [495552, 1, 576] pool, every layer). Used only to measure that baseline.
+ *  in  device uint8 [n_elems]; out device uint16 [n_elems]; both 16-byte aligned.
+ */
+int kv_pool_cast_bf16(const uint8_t* in, int64_t n_elems, void* out, qkvp_stream_t stream);
+
+/*
+ * qkvp_encode_f32 - the device rounding routines of kv_append_quant applied to raw FP32 values:
+ * fmt 1 -> E4M3 (nearest even, saturating at +-448, NaN -> 0x7F); fmt 2 -> E2M1 (nearest even,
+ * saturating at +-6, NaN -> 0x0). One code byte per input. Exposed so the rounding can be checked
+ * exhaustively against the CPU oracle.
+ */
+int qkvp_encode_f32(const float* x, int64_t n, int32_t fmt, uint8_t* codes, qkvp_stream_t stream);
+
+/* Static description of a status code; never NULL. */
+const char* qkvp_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int qkvp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKVP_H_ */

@@ -1,0 +1,328 @@
+// libqkvp C ABI: argument checks, the split-KV planner and kernel dispatch.
+//
+// Nothing here allocates device memory. mla_decode_plan stages its work table in a host vector
+// and copies it into the caller's workspace with one asynchronous copy on the caller's stream
+// (a pageable source is staged by the runtime before the call returns, so the vector may die).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "../../include/qkvp.h"
+#include "qkvp_internal.h"
+
+using namespace qkvp;
+
+namespace {
+
+constexpr uint64_t kAlign = 256;
+
+uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct TableLayout {
+  uint64_t segs, wptr, rptr, bytes;
+};
+
+TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch) {
+  TableLayout t;
+  t.segs = 0;
+  t.wptr = align_up(static_cast<uint64_t>(segments) * sizeof(Segment));
+  t.rptr = t.wptr + align_up(static_cast<uint64_t>(workers + 1) * 4);
+  t.bytes = t.rptr + align_up(static_cast<uint64_t>(batch + 1) * 4);
+  return t;
+}
+
+int query_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return sms;
+}
+
+// Balanced split of the batch's pages over the workers.
+//
+// Requests are laid end to end in request order, one unit per page (ceil(len / 64) pages each),
+// and worker w takes the contiguous run of pages [w * quota, (w + 1) * quota), quota =
+// ceil(total / workers), so no worker holds more than one page above the mean. Each worker's run is
+// cut at request boundaries and into pieces of at most `cap` pages, cap = total / min_splits when a
+// minimum number of splits is asked for; each piece is one segment. Segments therefore come in
+// request order, and the segments of one request are contiguous.
+struct Split {
+  std::vector<Segment> segs;
+  std::vector<int32_t> wptr, rptr;
+  int32_t split_reqs = 0, empty_reqs = 0, max_pages = 0, min_pages = 0, partials = 0;
+  int64_t total_pages = 0, total_tokens = 0;
+};
+
+void split_pages(const int32_t* indptr, const int32_t* len, int batch, int workers, int min_splits,
+                 Split& s) {
+  std::vector<int64_t> pages(batch), start(batch + 1, 0);
+  for (int r = 0; r < batch; ++r) {
+    pages[r] = (static_cast<int64_t>(len[r]) + kPage - 1) / kPage;
+    start[r + 1] = start[r] + pages[r];
+    s.total_tokens += len[r];
+  }
+  const int64_t total = start[batch];
+  s.total_pages = total;
+  const int64_t quota = total > 0 ? (total + workers - 1) / workers : 0;
+  int64_t cap = quota;
+  if (min_splits > 0 && total > 0) cap = std::max<int64_t>(1, std::min<int64_t>(quota, total / min_splits));
+  s.wptr.assign(workers + 1, 0);
+  s.max_pages = 0;
+  s.min_pages = total > 0 ? INT32_MAX : 0;
+  int r = 0;
+  for (int w = 0; w < workers; ++w) {
+    s.wptr[w] = static_cast<int32_t>(s.segs.size());
+    const int64_t a = std::min(total, w * quota), b = std::min(total, (w + 1) * quota);
+    s.max_pages = std::max<int32_t>(s.max_pages, static_cast<int32_t>(b - a));
+    if (total > 0) s.min_pages = std::min<int32_t>(s.min_pages, static_cast<int32_t>(b - a));
+    int64_t x = a;
+    while (x < b) {
+      while (r < batch && start[r + 1] <= x) ++r;
+      const int64_t y = std::min(b, start[r + 1]);
+      for (int64_t c = x; c < y; c += cap) {
+        const int64_t e = std::min(y, c + cap);
+        Segment g{};
+        g.req = r;
+        g.page_begin = static_cast<int32_t>(indptr[r] + (c - start[r]));
+        g.num_pages = static_cast<int32_t>(e - c);
+        const int64_t t0 = (c - start[r]) * kPage;
+        const int64_t t1 = std::min<int64_t>(len[r], (e - start[r]) * kPage);
+        g.num_tokens = static_cast<int32_t>(t1 - t0);
+        g.partial = 0;
+        s.segs.push_back(g);
+      }
+      x = y;
+    }
+  }
+  s.wptr[workers] = static_cast<int32_t>(s.segs.size());
+  // per-request segment ranges; requests with one segment write their output directly
+  s.rptr.assign(batch + 1, 0);
+  size_t k = 0;
+  int32_t part = 0;
+  for (int q = 0; q < batch; ++q) {
+    s.rptr[q] = static_cast<int32_t>(k);
+    size_t k0 = k;
+    while (k < s.segs.size() && s.segs[k].req == q) ++k;
+    const size_t n = k - k0;
+    if (n == 0) ++s.empty_reqs;
+    if (n >= 2) ++s.split_reqs;
+    for (size_t i = k0; i < k; ++i) s.segs[i].partial = n == 1 ? -1 : part++;
+  }
+  s.rptr[batch] = static_cast<int32_t>(k);
+  s.partials = part;
+}
+
+bool finite_float(float x) { return std::isfinite(x); }
+
+}  // namespace
+
+extern "C" {
+
+int qkvp_version(void) { return 100; }
+
+const char* qkvp_status_string(int status) {
+  switch (status) {
+    case QKVP_OK: return "ok";
+    case QKVP_E_INVALID: return "invalid argument";
+    case QKVP_E_UNSUPPORTED: return "unsupported configuration";
+    case QKVP_E_WORKSPACE: return "workspace missing or too small";
+    case QKVP_E_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int kv_append_quant(const void* src, int32_t src_dtype, int64_t n_tokens, const int64_t* slot_mapping,
+                    void* kv_data, uint8_t* kv_scale, int32_t kv_dtype, float global_scale,
+                    int32_t page_size, int64_t num_pages, qkvp_stream_t stream) {
+  if (n_tokens < 0 || num_pages < 0) return QKVP_E_INVALID;
+  if (src_dtype != QKVP_SRC_FP8_E4M3 && src_dtype != QKVP_SRC_BF16) return QKVP_E_UNSUPPORTED;
+  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4) return QKVP_E_UNSUPPORTED;
+  if (page_size != QKVP_PAGE_SIZE) return QKVP_E_UNSUPPORTED;
+  if (kv_dtype == QKVP_KV_FP8_E4M3) {
+    if (kv_scale != nullptr || global_scale != 1.0f) return QKVP_E_INVALID;
+  } else {
+    if (kv_scale == nullptr || !finite_float(global_scale) || !(global_scale > 0.0f)) return QKVP_E_INVALID;
+    if (!aligned(kv_scale, 16)) return QKVP_E_INVALID;
+  }
+  if (n_tokens == 0) return QKVP_OK;
+  if (!src || !slot_mapping || !kv_data) return QKVP_E_INVALID;
+  if (!aligned(src, 16) || !aligned(kv_data, 16) || !aligned(slot_mapping, 8)) return QKVP_E_INVALID;
+  if (num_pages > (INT64_MAX / page_size)) return QKVP_E_INVALID;
+  cudaError_t e = launch_append(src, src_dtype, n_tokens, slot_mapping, kv_data, kv_scale, kv_dtype,
+                                global_scale, num_pages * page_size, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
+}
+
+int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int32_t batch,
+                    int32_t num_heads, int32_t page_size, int32_t kv_dtype, int32_t num_sms,
+                    int32_t min_splits, int32_t algo, void* workspace, uint64_t workspace_bytes,
+                    qkvp_stream_t stream, qkvp_plan* plan) {
+  if (!plan) return QKVP_E_INVALID;
+  std::memset(plan, 0, sizeof(*plan));
+  if (batch < 0 || min_splits < 0) return QKVP_E_INVALID;
+  if (batch > 0 && (!kv_indptr_host || !kv_len_host)) return QKVP_E_INVALID;
+  if (page_size != QKVP_PAGE_SIZE) return QKVP_E_UNSUPPORTED;
+  if (num_heads < 16 || num_heads > 128 || num_heads % 16) return QKVP_E_UNSUPPORTED;
+  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16)
+    return QKVP_E_UNSUPPORTED;
+  if (algo == QKVP_ALGO_AUTO) algo = QKVP_ALGO_MMA_SYNC;
+  if (algo != QKVP_ALGO_MMA_SYNC) return QKVP_E_UNSUPPORTED;
+  if (batch > 0 && kv_indptr_host[0] != 0) return QKVP_E_INVALID;
+  for (int r = 0; r < batch; ++r) {
+    const int64_t np = static_cast<int64_t>(kv_indptr_host[r + 1]) - kv_indptr_host[r];
+    if (np < 0 || kv_len_host[r] < 0) return QKVP_E_INVALID;
+    if ((static_cast<int64_t>(kv_len_host[r]) + page_size - 1) / page_size > np) return QKVP_E_INVALID;
+  }
+  if (num_sms <= 0) {
+    num_sms = query_sms();
+    if (num_sms <= 0) return QKVP_E_CUDA;
+  }
+  const int hc = mma_heads_per_cta(num_heads);
+  if (hc == 0) return QKVP_E_UNSUPPORTED;
+  const int cpw = num_heads / hc;
+  const int workers = std::max(1, num_sms / cpw);
+
+  Split s;
+  split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, s);
+  const TableLayout t = table_layout(static_cast<int64_t>(s.segs.size()), workers, batch);
+  plan->batch = batch;
+  plan->num_heads = num_heads;
+  plan->page_size = page_size;
+  plan->kv_dtype = kv_dtype;
+  plan->algo = algo;
+  plan->num_workers = workers;
+  plan->ctas_per_worker = cpw;
+  plan->num_segments = static_cast<int32_t>(s.segs.size());
+  plan->num_split_requests = s.split_reqs;
+  plan->num_empty_requests = s.empty_reqs;
+  plan->max_worker_pages = s.max_pages;
+  plan->min_worker_pages = s.min_pages;
+  plan->num_partials = s.partials;
+  plan->total_pages = s.total_pages;
+  plan->total_tokens = s.total_tokens;
+  plan->table_bytes = t.bytes;
+  plan->partial_o_offset = t.bytes;
+  plan->partial_lse_offset = t.bytes + align_up(static_cast<uint64_t>(s.partials) * num_heads * QKVP_V_DIM * 4);
+  plan->workspace_bytes = plan->partial_lse_offset + align_up(static_cast<uint64_t>(s.partials) * num_heads * 4);
+  if (workspace == nullptr) return QKVP_OK;  // size query: no device work
+  if (workspace_bytes < plan->workspace_bytes || !aligned(workspace, kAlign)) {
+    const uint64_t need = plan->workspace_bytes;
+    std::memset(plan, 0, sizeof(*plan));
+    plan->workspace_bytes = need;
+    return QKVP_E_WORKSPACE;
+  }
+  std::vector<uint8_t> blob(t.bytes, 0);
+  if (!s.segs.empty()) std::memcpy(blob.data() + t.segs, s.segs.data(), s.segs.size() * sizeof(Segment));
+  std::memcpy(blob.data() + t.wptr, s.wptr.data(), s.wptr.size() * 4);
+  std::memcpy(blob.data() + t.rptr, s.rptr.data(), s.rptr.size() * 4);
+  cudaError_t e = cudaMemcpyAsync(workspace, blob.data(), blob.size(), cudaMemcpyHostToDevice,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return QKVP_E_CUDA;
+  plan->magic = kPlanMagic;
+  return QKVP_OK;
+}
+
+namespace {
+
+int check_run_args(const qkvp_plan* plan, int64_t num_pages, float sm_scale, float global_scale,
+                   void* workspace, uint64_t workspace_bytes) {
+  if (!plan || plan->magic != kPlanMagic) return QKVP_E_INVALID;
+  if (!workspace || workspace_bytes < plan->workspace_bytes || !aligned(workspace, kAlign)) return QKVP_E_WORKSPACE;
+  if (num_pages < 0 || !finite_float(sm_scale)) return QKVP_E_INVALID;
+  if (plan->kv_dtype == QKVP_KV_NVFP4) {
+    if (!finite_float(global_scale) || !(global_scale > 0.0f)) return QKVP_E_INVALID;
+  } else if (global_scale != 1.0f) {
+    return QKVP_E_INVALID;
+  }
+  return QKVP_OK;
+}
+
+DecodeArgs make_args(const qkvp_plan* plan, const void* q, const void* kv_data, const uint8_t* kv_scale,
+                     int64_t num_pages, const int32_t* kv_indices, float sm_scale, float global_scale,
+                     void* out, float* lse, void* workspace) {
+  const TableLayout t = table_layout(plan->num_segments, plan->num_workers, plan->batch);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.kv = static_cast<const uint8_t*>(kv_data);
+  a.kv_scale = kv_scale;
+  a.num_pages = num_pages;
+  a.kv_indices = kv_indices;
+  a.segs = reinterpret_cast<const Segment*>(ws + t.segs);
+  a.worker_ptr = reinterpret_cast<const int32_t*>(ws + t.wptr);
+  a.req_seg_ptr = reinterpret_cast<const int32_t*>(ws + t.rptr);
+  a.part_o = reinterpret_cast<float*>(ws + plan->partial_o_offset);
+  a.part_lse = reinterpret_cast<float*>(ws + plan->partial_lse_offset);
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.batch = plan->batch;
+  a.heads = plan->num_heads;
+  a.num_workers = plan->num_workers;
+  a.ctas_per_worker = plan->ctas_per_worker;
+  a.num_segments = plan->num_segments;
+  a.kv_dtype = plan->kv_dtype;
+  a.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * global_scale * 1.4426950408889634);
+  a.out_scale = global_scale;
+  return a;
+}
+
+}  // namespace
+
+int mla_decode_attend(const qkvp_plan* plan, const void* q, const void* kv_data, const uint8_t* kv_scale,
+                      int64_t num_pages, const int32_t* kv_indices, float sm_scale, float global_scale,
+                      void* out, float* lse, void* workspace, uint64_t workspace_bytes,
+                      qkvp_stream_t stream) {
+  int st = check_run_args(plan, num_pages, sm_scale, global_scale, workspace, workspace_bytes);
+  if (st != QKVP_OK) return st;
+  if (plan->batch == 0 || plan->num_segments == 0) return QKVP_OK;
+  if (!q || !out || !aligned(q, 16) || !aligned(out, 4) || (lse && !aligned(lse, 4))) return QKVP_E_INVALID;
+  if (!kv_data || !kv_indices || !aligned(kv_data, 16) || !aligned(kv_indices, 4)) return QKVP_E_INVALID;
+  if (plan->kv_dtype == QKVP_KV_NVFP4 && (!kv_scale || !aligned(kv_scale, 16))) return QKVP_E_INVALID;
+  const DecodeArgs a = make_args(plan, q, kv_data, kv_scale, num_pages, kv_indices, sm_scale,
+                                 global_scale, out, lse, workspace);
+  cudaError_t e = launch_decode_mma(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
+}
+
+int mla_decode_combine(const qkvp_plan* plan, float global_scale, void* out, float* lse,
+                       void* workspace, uint64_t workspace_bytes, qkvp_stream_t stream) {
+  int st = check_run_args(plan, 0, 0.0f, global_scale, workspace, workspace_bytes);
+  if (st != QKVP_OK) return st;
+  if (plan->batch == 0 || (plan->num_split_requests == 0 && plan->num_empty_requests == 0)) return QKVP_OK;
+  if (!out || !aligned(out, 4) || (lse && !aligned(lse, 4))) return QKVP_E_INVALID;
+  const DecodeArgs a = make_args(plan, nullptr, nullptr, nullptr, 0, nullptr, 0.0f, global_scale,
+                                 out, lse, workspace);
+  cudaError_t e = launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
+}
+
+int mla_decode_run(const qkvp_plan* plan, const void* q, const void* kv_data, const uint8_t* kv_scale,
+                   int64_t num_pages, const int32_t* kv_indices, float sm_scale, float global_scale,
+                   void* out, float* lse, void* workspace, uint64_t workspace_bytes,
+                   qkvp_stream_t stream) {
+  int st = mla_decode_attend(plan, q, kv_data, kv_scale, num_pages, kv_indices, sm_scale, global_scale,
+                             out, lse, workspace, workspace_bytes, stream);
+  if (st != QKVP_OK) return st;
+  return mla_decode_combine(plan, global_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int kv_pool_cast_bf16(const uint8_t* in, int64_t n_elems, void* out, qkvp_stream_t stream) {
+  if (n_elems < 0 || n_elems % 16) return QKVP_E_INVALID;
+  if (n_elems == 0) return QKVP_OK;
+  if (!in || !out || !aligned(in, 16) || !aligned(out, 16)) return QKVP_E_INVALID;
+  cudaError_t e = launch_cast(in, n_elems, static_cast<uint16_t*>(out), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
+}
+
+int qkvp_encode_f32(const float* x, int64_t n, int32_t fmt, uint8_t* codes, qkvp_stream_t stream) {
+  if (n < 0 || (fmt != 1 && fmt != 2)) return QKVP_E_INVALID;
+  if (n == 0) return QKVP_OK;
+  if (!x || !codes || !aligned(x, 4)) return QKVP_E_INVALID;
+  cudaError_t e = launch_encode(x, n, fmt, codes, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,373 @@
+// Split-KV paged MLA decode with warp-level mma.sync (FP16 operands, FP32 accumulate).
+//
+// The attention computed is the one of the pages' plan()/run() call ("The Smoking Gun", section
+// "What Message 1408 Actually Reveals"): per request and head, softmax(sm_scale * q . k) v over the
+// request's tokens, K = the whole 576-wide latent and V = its first 512 dims. Pages are read in
+// their stored format and dequantized in registers ("SGLang x Qwen x NVIDIA ... NVFP4 KV Cache",
+// section "SGLang implementation", item 3); the global NVFP4 scale is folded into the logit scale
+// and the output scale.
+//
+// Operand precision. The pages compute in BF16. Here both products take FP16 operands: every
+// dequantized K/V value is exact in FP16, and the softmax probabilities P keep 11 mantissa bits
+// instead of 8, which is what holds the output within 2e-2 of the FP64 result when a few tokens
+// carry large value channels (|O| ~ 100). Q arrives in BF16 and is converted to FP16 once per CTA
+// after multiplying by a power of two 2^-s chosen from the largest |q| of the CTA's heads (so no
+// value overflows FP16); 2^s is folded into the logit scale, which keeps the product exact.
+//
+// Decomposition. A worker owns a list of segments (request, page range). Each worker runs
+// H / HC CTAs, one per group of HC query heads (HC = 16..64). Within a CTA, warps come in pairs
+// that own the same 16 heads: warp (g, 0) holds output dims 0..255 and computes the logits over
+// latent dims 0..287, warp (g, 1) holds output dims 256..511 and computes the logits over dims
+// 288..575; the two partial logit tiles are summed through shared memory in a fixed order, so both
+// warps see bit-identical logits, maxima and probabilities. Per page:
+//   cp.async raw page -> smem  |  dequantize -> FP16 tile [64 tokens][576]  |  S = Q K^T (mma.sync)
+//   |  exchange + online softmax (FP32, base 2)  |  O += P V (mma.sync, P from registers).
+// The next page's raw bytes are fetched while the current page is multiplied.
+#include <cfloat>
+#include <cstdint>
+
+#include "qkvp_device.cuh"
+#include "qkvp_internal.h"
+
+namespace qkvp {
+namespace {
+
+constexpr int kRow = kLatent + 8;          // padded smem row of the 16-bit tiles (1168 bytes)
+constexpr int kRowBytes = kRow * 2;
+
+template <int KV>
+constexpr int raw_bytes() {
+  return KV == KV_FP8 ? kPage * kLatent : (KV == KV_NVFP4 ? kPage * (kPacked + kScales) : 0);
+}
+
+template <int KV, int HC>
+constexpr int smem_bytes() {
+  return HC * kRowBytes + kPage * kRowBytes + raw_bytes<KV>() + (HC / 16) * 2 * 32 * 32 * 4 + 16;
+}
+
+// Fetch the raw bytes of one page (or, for BF16, the page itself) with cp.async.
+template <int KV, int NT>
+__device__ __forceinline__ void issue_page(const DecodeArgs& a, int64_t page, int valid,
+                                           uint32_t s_raw, uint32_t s_kv, int tid) {
+  if (page < 0 || page >= a.num_pages) return;
+  if (KV == KV_FP8) {
+    const uint8_t* g = a.kv + page * (kPage * kLatent);
+    for (int c = tid; c < valid * (kLatent / 16); c += NT) dev::cp_async16(s_raw + c * 16, g + c * 16);
+  } else if (KV == KV_NVFP4) {
+    const uint8_t* g = a.kv + page * (kPage * kPacked);
+    for (int c = tid; c < valid * (kPacked / 16); c += NT) dev::cp_async16(s_raw + c * 16, g + c * 16);
+    const uint8_t* gs = a.kv_scale + page * (kPage * kScales);
+    for (int c = tid; c < kPage * kScales / 16; c += NT)
+      dev::cp_async16(s_raw + kPage * kPacked + c * 16, gs + c * 16);
+  } else {
+    const uint8_t* g = a.kv + page * (kPage * kLatent * 2);
+    for (int c = tid; c < valid * (kLatent * 2 / 16); c += NT) {
+      const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
+      dev::cp_async16(s_kv + row * kRowBytes + ch * 16, g + c * 16);
+    }
+  }
+  dev::cp_async_commit();
+}
+
+// Raw page bytes in smem -> FP16 tile rows [0, valid); rows >= valid (or a bad page) -> zeros.
+template <int KV, int NT>
+__device__ __forceinline__ void dequant_page(const uint8_t* s_raw, uint8_t* s_kv, int valid, int tid) {
+  if (KV == KV_FP8) {
+    for (int c = tid; c < valid * (kLatent / 16); c += NT) {
+      const int row = c / (kLatent / 16), ch = c % (kLatent / 16);
+      const uint4 v = *reinterpret_cast<const uint4*>(s_raw + c * 16);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        o[2 * k] = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+        o[2 * k + 1] = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
+      }
+      uint4* dst = reinterpret_cast<uint4*>(s_kv + row * kRowBytes + ch * 32);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  } else if (KV == KV_NVFP4) {
+    const uint8_t* s_sc = s_raw + kPage * kPacked;
+    for (int c = tid; c < valid * (kPacked / 16); c += NT) {
+      const int row = c / (kPacked / 16), ch = c % (kPacked / 16);
+      const uint4 v = *reinterpret_cast<const uint4*>(s_raw + c * 16);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t sa = s_sc[row * kScales + 2 * ch], sb = s_sc[row * kScales + 2 * ch + 1];
+      const uint32_t ha = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sa | (sa << 8)));
+      const uint32_t hb = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
+      uint32_t o[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) o[4 * k + b] = dev::nvfp4x2_to_f16x2((w[k] >> (8 * b)) & 0xFFu, k < 2 ? ha : hb);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(s_kv + row * kRowBytes + ch * 64);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      dst[2] = make_uint4(o[8], o[9], o[10], o[11]);
+      dst[3] = make_uint4(o[12], o[13], o[14], o[15]);
+    }
+  } else {
+    // BF16 pool: the rows were copied in as BF16; convert them to FP16 in place
+    for (int c = tid; c < valid * (kLatent * 2 / 16); c += NT) {
+      const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
+      uint4* p = reinterpret_cast<uint4*>(s_kv + row * kRowBytes + ch * 16);
+      const uint4 v = *p;
+      *p = make_uint4(dev::bf16x2_to_f16x2(v.x), dev::bf16x2_to_f16x2(v.y), dev::bf16x2_to_f16x2(v.z),
+                      dev::bf16x2_to_f16x2(v.w));
+    }
+  }
+  // zero the rows past the valid tokens (their bytes are never read into the result)
+  for (int c = tid; c < (kPage - valid) * (kLatent * 2 / 16); c += NT) {
+    const int row = valid + c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
+    *reinterpret_cast<uint4*>(s_kv + row * kRowBytes + ch * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int KV, int HC>
+__global__ void __launch_bounds__(HC * 4, 1) decode_mma_kernel(const DecodeArgs a) {
+  constexpr int NG = HC / 16;       // 16-head groups in this CTA
+  constexpr int NT = NG * 64;       // two warps per group
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* s_q = smem;
+  uint8_t* s_kv = s_q + HC * kRowBytes;
+  uint8_t* s_raw = s_kv + kPage * kRowBytes;
+  float* s_x = reinterpret_cast<float*>(s_raw + raw_bytes<KV>());
+  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + (HC / 16) * 2 * 1024);
+  const uint32_t a_q = dev::smem_u32(s_q), a_kv = dev::smem_u32(s_kv), a_raw = dev::smem_u32(s_raw);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = warp >> 1, half = warp & 1;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int worker = blockIdx.x / a.ctas_per_worker;
+  const int h0 = (blockIdx.x % a.ctas_per_worker) * HC;
+  const int seg_b = a.worker_ptr[worker], seg_e = a.worker_ptr[worker + 1];
+
+  // ldmatrix lane addresses (bytes, relative to the tile bases)
+  const uint32_t q_lane = ((grp * 16 + (lane & 15)) * kRow + (lane >> 4) * 8) * 2;
+  const uint32_t k_lane = (((lane & 7) + ((lane >> 4) << 3)) * kRow + ((lane >> 3) & 1) * 8) * 2;
+  const uint32_t v_lane = (((lane & 7) + ((lane >> 3) & 1) * 8) * kRow + half * 256 + (lane >> 4) * 8) * 2;
+  float* x_mine = s_x + (grp * 2 + half) * 1024;
+  float* x_peer = s_x + (grp * 2 + (half ^ 1)) * 1024;
+
+  int cur_req = -1;
+  float q_scale_log2 = a.scale_log2;
+  for (int si = seg_b; si < seg_e; ++si) {
+    const Segment seg = a.segs[si];
+    __syncthreads();  // the previous segment is done with s_q / s_kv / s_raw
+    if (seg.req != cur_req) {
+      const uint8_t* gq = reinterpret_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(seg.req) * a.heads + h0) * kLatent * 2;
+      for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
+        const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
+        dev::cp_async16(a_q + row * kRowBytes + ch * 16, gq + static_cast<int64_t>(row) * kLatent * 2 + ch * 16);
+      }
+      dev::cp_async_commit();
+      if (tid == 0) *s_qmax = 0u;
+      dev::cp_async_wait_all();
+      __syncthreads();
+      // largest |q| of this CTA's heads, as BF16 magnitude bits (integer order = magnitude order)
+      uint32_t mx = 0;
+      for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
+        const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
+        const uint4 v = *reinterpret_cast<const uint4*>(s_q + row * kRowBytes + ch * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+      }
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      if (lane == 0) atomicMax(s_qmax, mx);
+      __syncthreads();
+      // q * 2^-s puts the largest |q| in [2^14, 2^15); inf / NaN / all-zero tiles keep s = 0
+      const uint32_t qm = *s_qmax;
+      int sh = 0;
+      if (qm != 0u && qm < 0x7F80u) sh = max(-100, min(113, static_cast<int>(qm >> 7) - 127 - 14));
+      const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+      q_scale_log2 = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+      for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
+        const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
+        uint4* p = reinterpret_cast<uint4*>(s_q + row * kRowBytes + ch * 16);
+        const uint4 v = *p;
+        *p = make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
+                        dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down));
+      }
+      cur_req = seg.req;
+      // the conversion is made visible to every warp by the barrier before the first page
+    }
+    float o[32][4];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.0f, 0.0f};
+
+    int64_t page = a.kv_indices[seg.page_begin];
+    if (KV != KV_BF16) issue_page<KV, NT>(a, page, min(kPage, seg.num_tokens), a_raw, a_kv, tid);
+    for (int j = 0; j < seg.num_pages; ++j) {
+      const int valid = min(kPage, seg.num_tokens - j * kPage);
+      const bool page_ok = page >= 0 && page < a.num_pages;
+      if (KV == KV_BF16) issue_page<KV, NT>(a, page, valid, a_raw, a_kv, tid);
+      dev::cp_async_wait_all();
+      __syncthreads();
+      dequant_page<KV, NT>(s_raw, s_kv, page_ok ? valid : 0, tid);
+      __syncthreads();
+      if (j + 1 < seg.num_pages) {
+        page = a.kv_indices[seg.page_begin + j + 1];
+        if (KV != KV_BF16) issue_page<KV, NT>(a, page, min(kPage, seg.num_tokens - (j + 1) * kPage), a_raw, a_kv, tid);
+      }
+      const int live = page_ok ? valid : 0;
+
+      // ---- S partial = Q[:, my dims] K[:, my dims]^T  (16 heads x 64 tokens) ----
+      float s[8][4];
+#pragma unroll
+      for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
+#pragma unroll 2
+      for (int ks = 0; ks < 18; ++ks) {
+        const int kk = half * 288 + ks * 16;
+        uint32_t a0, a1, a2, a3;
+        dev::ldsm_x4(a_q + q_lane + kk * 2, a0, a1, a2, a3);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          uint32_t b0, b1, b2, b3;
+          dev::ldsm_x4(a_kv + k_lane + (p * 16 * kRow + kk) * 2, b0, b1, b2, b3);
+          dev::mma_f16(s[2 * p], a0, a1, a2, a3, b0, b1);
+          dev::mma_f16(s[2 * p + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+      // ---- exchange the partial logits with the peer warp; sum in a fixed order ----
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x_mine[(n * 4 + i) * 32 + lane] = s[n][i];
+      dev::named_bar_sync(1 + grp, 64);
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float peer = x_peer[(n * 4 + i) * 32 + lane];
+          s[n][i] = half == 0 ? (s[n][i] + peer) : (peer + s[n][i]);
+        }
+      // ---- online softmax in base 2 (rows g8 and g8 + 8 of the 16 heads) ----
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = n * 8 + 2 * t4 + (i & 1);
+          const float v = tok < live ? s[n][i] * q_scale_log2 : -INFINITY;
+          s[n][i] = v;
+          mx[i >> 1] = fmaxf(mx[i >> 1], v);
+        }
+      float alpha[2], mref[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+        const float m_new = fmaxf(m_r[r], mx[r]);
+        mref[r] = m_new == -INFINITY ? 0.0f : m_new;
+        alpha[r] = dev::fast_exp2(m_r[r] - mref[r]);
+        m_r[r] = m_new;
+        l_r[r] *= alpha[r];
+      }
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float p = dev::fast_exp2(s[n][i] - mref[i >> 1]);
+          s[n][i] = p;
+          l_r[i >> 1] += p;
+        }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        o[i][0] *= alpha[0]; o[i][1] *= alpha[0];
+        o[i][2] *= alpha[1]; o[i][3] *= alpha[1];
+      }
+      // ---- O[:, my 256 dims] += P V ----
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        const uint32_t pa0 = dev::pack_f16x2(s[2 * kt][0], s[2 * kt][1]);
+        const uint32_t pa1 = dev::pack_f16x2(s[2 * kt][2], s[2 * kt][3]);
+        const uint32_t pa2 = dev::pack_f16x2(s[2 * kt + 1][0], s[2 * kt + 1][1]);
+        const uint32_t pa3 = dev::pack_f16x2(s[2 * kt + 1][2], s[2 * kt + 1][3]);
+#pragma unroll
+        for (int vp = 0; vp < 16; ++vp) {
+          uint32_t b0, b1, b2, b3;
+          dev::ldsm_x4_t(a_kv + v_lane + (kt * 16 * kRow + vp * 16) * 2, b0, b1, b2, b3);
+          dev::mma_f16(o[2 * vp], pa0, pa1, pa2, pa3, b0, b1);
+          dev::mma_f16(o[2 * vp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+      }
+      __syncthreads();  // s_kv and the exchange buffers are reused by the next page
+    }
+
+    // ---- epilogue: normalise; write the output directly or a split partial ----
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
+      l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
+    }
+    const float inv[2] = {l_r[0] > 0.0f ? 1.0f / l_r[0] : 0.0f, l_r[1] > 0.0f ? 1.0f / l_r[1] : 0.0f};
+    const float lse2[2] = {l_r[0] > 0.0f ? m_r[0] + __log2f(l_r[0]) : -INFINITY,
+                           l_r[1] > 0.0f ? m_r[1] + __log2f(l_r[1]) : -INFINITY};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int head = h0 + grp * 16 + g8 + 8 * r;
+      if (seg.partial < 0) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + (static_cast<int64_t>(seg.req) * a.heads + head) * kDv + half * 256);
+        const float sc = inv[r] * a.out_scale;
+#pragma unroll
+        for (int nt = 0; nt < 32; ++nt) dst[(nt * 8 + 2 * t4) / 2] = dev::pack_bf16x2(o[nt][2 * r] * sc, o[nt][2 * r + 1] * sc);
+        if (half == 0 && t4 == 0 && a.lse) a.lse[static_cast<int64_t>(seg.req) * a.heads + head] = lse2[r] * 0.69314718055994531f;
+      } else {
+        float2* dst = reinterpret_cast<float2*>(a.part_o + (static_cast<int64_t>(seg.partial) * a.heads + head) * kDv + half * 256);
+#pragma unroll
+        for (int nt = 0; nt < 32; ++nt) dst[(nt * 8 + 2 * t4) / 2] = make_float2(o[nt][2 * r] * inv[r], o[nt][2 * r + 1] * inv[r]);
+        if (half == 0 && t4 == 0) a.part_lse[static_cast<int64_t>(seg.partial) * a.heads + head] = lse2[r];
+      }
+    }
+  }
+}
+
+template <int KV, int HC>
+cudaError_t launch_kv_hc(const DecodeArgs& a, cudaStream_t s) {
+  constexpr int smem = smem_bytes<KV, HC>();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<KV, HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const unsigned grid = static_cast<unsigned>(a.num_workers * a.ctas_per_worker);
+  decode_mma_kernel<KV, HC><<<grid, HC * 4, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int KV>
+cudaError_t launch_kv(const DecodeArgs& a, cudaStream_t s) {
+  switch (mma_heads_per_cta(a.heads)) {
+    case 16: return launch_kv_hc<KV, 16>(a, s);
+    case 32: return launch_kv_hc<KV, 32>(a, s);
+    case 48: return launch_kv_hc<KV, 48>(a, s);
+    case 64: return launch_kv_hc<KV, 64>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int mma_heads_per_cta(int heads) {
+  if (heads < 16 || heads > 128 || heads % 16) return 0;
+  for (int hc : {64, 48, 32, 16})
+    if (heads % hc == 0) return hc;
+  return 0;
+}
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
+  if (a.num_segments == 0) return cudaSuccess;
+  switch (a.kv_dtype) {
+    case KV_FP8: return launch_kv<KV_FP8>(a, s);
+    case KV_NVFP4: return launch_kv<KV_NVFP4>(a, s);
+    case KV_BF16: return launch_kv<KV_BF16>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qkvp

@@ -1,0 +1,66 @@
+// Internal declarations shared by the translation units of libqkvp (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace qkvp {
+
+constexpr int kLatent = 576;            // 512 nope + 64 rope
+constexpr int kDv = 512;                // V = the first 512 latent dims
+constexpr int kPage = 64;               // tokens per page
+constexpr int kPacked = kLatent / 2;    // NVFP4 data bytes per token (two E2M1 codes per byte)
+constexpr int kScales = kLatent / 16;   // NVFP4 E4M3 block scales per token
+constexpr uint64_t kPlanMagic = 0x716b76702d706c31ull;
+
+enum : int { KV_FP8 = 1, KV_NVFP4 = 2, KV_BF16 = 3 };
+enum : int { SRC_FP8 = 1, SRC_BF16 = 2 };
+enum : int { ALGO_AUTO = 0, ALGO_MMA = 1, ALGO_TC = 2 };
+
+// One piece of one request's page list, processed by one worker from start to end. Segments are
+// stored in request order; a request whose pages form a single segment is written straight to the
+// output (partial < 0), otherwise each segment writes a normalised FP32 partial and its
+// log2-sum-exp, merged by the combine kernel.
+struct Segment {
+  int32_t req;
+  int32_t page_begin;   // index into kv_indices of the first page
+  int32_t num_pages;
+  int32_t num_tokens;   // tokens covered (the last page may be partial)
+  int32_t partial;      // partial slot, or -1 for a direct write
+  int32_t pad[3];
+};
+static_assert(sizeof(Segment) == 32, "segment layout");
+
+struct DecodeArgs {
+  const uint16_t* q;          // bf16 [B][H][576]
+  const uint8_t* kv;          // pool (fp8 / nvfp4 data / bf16)
+  const uint8_t* kv_scale;    // nvfp4 block scales
+  int64_t num_pages;
+  const int32_t* kv_indices;
+  const Segment* segs;
+  const int32_t* worker_ptr;  // [num_workers + 1]
+  const int32_t* req_seg_ptr; // [batch + 1]
+  float* part_o;              // [num_segments][H][512]
+  float* part_lse;            // [num_segments][H], log2 domain
+  uint16_t* out;              // bf16 [B][H][512]
+  float* lse;                 // [B][H] natural log, may be null
+  int batch, heads, num_workers, ctas_per_worker, num_segments, kv_dtype;
+  float scale_log2;           // sm_scale * g * log2(e)
+  float out_scale;            // g
+};
+
+cudaError_t launch_append(const void* src, int src_dtype, int64_t n, const int64_t* slots,
+                          void* kv_data, uint8_t* kv_scale, int kv_dtype, float g,
+                          int64_t num_slots, cudaStream_t s);
+cudaError_t launch_encode(const float* x, int64_t n, int fmt, uint8_t* codes, cudaStream_t s);
+cudaError_t launch_cast(const uint8_t* in, int64_t n, uint16_t* out, cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
+
+// Heads per CTA of the mma.sync kernel for a head count (0 if unsupported).
+int mma_heads_per_cta(int heads);
+
+}  // namespace qkvp

@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads and exports every function qkvp.h declares; argument
+checks fail before any launch; the planner's split is balanced and honours min_splits."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import quantized_kv_paged_gb300 as q
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_kv_paged_gb300 import build
+    build.build()
+    return q.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "qkvp.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(q.EXPORTS) == set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    assert q.status_string(0) == "ok"
+    for s in (-1, -2, -3, -4, 7):
+        assert q.status_string(s)
+    assert q.qkvp_version() >= 100
+
+
+def plan(indptr, lens, heads=128, kv=q.KV_FP8_E4M3, sms=152, min_splits=0, algo=0, page_size=64):
+    return q.mla_decode_plan(indptr, lens, heads, kv, num_sms=sms, min_splits=min_splits,
+                             algo=algo, page_size=page_size, raise_on_error=False)
+
+
+def test_plan_rejects_bad_arguments(lib):
+    ok_ptr, ok_len = np.array([0, 2], np.int32), np.array([100], np.int32)
+    assert plan(ok_ptr, ok_len).status == q.QKVP_OK
+    assert plan(ok_ptr, ok_len, page_size=32).status == q.QKVP_E_UNSUPPORTED
+    for h in (8, 24 + 1, 144, 0):
+        assert plan(ok_ptr, ok_len, heads=h).status == q.QKVP_E_UNSUPPORTED
+    assert plan(ok_ptr, ok_len, kv=9).status == q.QKVP_E_UNSUPPORTED
+    assert plan(np.array([1, 3], np.int32), ok_len).status == q.QKVP_E_INVALID       # indptr[0] != 0
+    assert plan(np.array([0, 1], np.int32), ok_len).status == q.QKVP_E_INVALID       # 100 tokens, 1 page
+    assert plan(np.array([0, 2], np.int32), np.array([-1], np.int32)).status == q.QKVP_E_INVALID
+    assert plan(np.array([0, 2, 1], np.int32), np.array([5, 5], np.int32)).status == q.QKVP_E_INVALID
+    assert plan(ok_ptr, ok_len, min_splits=-1).status == q.QKVP_E_INVALID
+    assert plan(ok_ptr, ok_len, algo=7).status == q.QKVP_E_UNSUPPORTED
+
+
+def test_plan_workspace_too_small_reports_size(lib):
+    ptr, lens = np.array([0, 512, 1024], np.int32), np.array([32768, 32768], np.int32)
+    p = plan(ptr, lens)
+    st = lib.mla_decode_plan(ptr.ctypes.data, lens.ctypes.data, 2, 128, 64, 1, 152, 0, 0,
+                             ctypes.c_void_p(256), 64, None, ctypes.byref(p))
+    assert st == q.QKVP_E_WORKSPACE and p.workspace_bytes > 64
+
+
+def test_split_is_balanced_and_covers_every_page(lib):
+    lens = np.array([32768] * 44, np.int32)
+    ptr = np.concatenate([[0], np.cumsum((lens + 63) // 64)]).astype(np.int32)
+    p = plan(ptr, lens)
+    assert p.total_pages == 44 * 512 and p.total_tokens == 44 * 32768
+    assert p.ctas_per_worker * p.num_workers <= 152
+    # makespan is the ceiling of the mean: no worker holds more than one page above it
+    assert p.max_worker_pages == -(-p.total_pages // p.num_workers)
+    assert p.min_worker_pages >= p.total_pages - (p.num_workers - 1) * p.max_worker_pages
+    assert p.num_segments >= 44 and p.workspace_bytes >= p.num_partials * 128 * 512 * 4
+
+
+def test_min_splits_spreads_one_long_request(lib):
+    lens = np.array([1 << 20], np.int32)
+    ptr = np.array([0, 16384], np.int32)
+    p = plan(ptr, lens, min_splits=148)
+    assert p.num_segments >= 148 and p.num_split_requests == 1 and p.num_partials == p.num_segments
+    p0 = plan(ptr, lens, min_splits=0)
+    assert p0.num_segments == p0.num_workers
+
+
+def test_ragged_and_empty_requests(lib):
+    lens = np.array([0, 1, 64, 65, 0, 1000], np.int32)
+    ptr = np.concatenate([[0], np.cumsum((lens + 63) // 64 + 1)]).astype(np.int32)   # 1 spare page each
+    p = plan(ptr, lens, heads=16, sms=4)
+    assert p.num_empty_requests == 2
+    assert p.total_pages == sum((int(l) + 63) // 64 for l in lens)
+    assert p.num_workers == 4 and p.ctas_per_worker == 1
+
+
+def test_run_and_append_reject_before_launch(lib):
+    p = plan(np.array([0, 2], np.int32), np.array([100], np.int32))
+    # a size-only plan carries no upload: run refuses it
+    st = lib.mla_decode_run(ctypes.byref(p), 16, 16, None, 10, 16, 0.1, 1.0, 16, None, 256,
+                            1 << 30, None)
+    assert st == q.QKVP_E_INVALID
+    f = lib.kv_append_quant
+    assert f(16, 1, 4, 16, 16, 16, 1, 1.0, 64, 10, None) == q.QKVP_E_INVALID      # FP8 with scale pool
+    assert f(16, 1, 4, 16, 16, None, 1, 2.0, 64, 10, None) == q.QKVP_E_INVALID    # FP8 with g != 1
+    assert f(16, 1, 4, 16, 16, None, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID    # NVFP4 without scales
+    assert f(16, 1, 4, 16, 16, 16, 2, 0.0, 64, 10, None) == q.QKVP_E_INVALID      # g = 0
+    assert f(16, 1, 4, 16, 16, 16, 2, float("nan"), 64, 10, None) == q.QKVP_E_INVALID
+    assert f(16, 1, 4, 16, 16, 16, 3, 1.0, 64, 10, None) == q.QKVP_E_UNSUPPORTED  # BF16 pool
+    assert f(16, 1, 4, 16, 16, 16, 2, 1.0, 32, 10, None) == q.QKVP_E_UNSUPPORTED  # page size
+    assert f(None, 1, 4, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID
+    assert f(17, 1, 4, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID      # misaligned source
+    assert f(16, 1, -1, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID
+    assert f(16, 1, 0, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_OK              # nothing to do
+    assert lib.kv_pool_cast_bf16(16, 17, 16, None) == q.QKVP_E_INVALID
+    assert lib.qkvp_encode_f32(16, 4, 3, 16, None) == q.QKVP_E_INVALID
