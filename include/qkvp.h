@@ -198,6 +198,35 @@ int mla_decode_combine(const qkvp_plan* plan, float global_scale, void* out, flo
                        void* workspace, uint64_t workspace_bytes, qkvp_stream_t stream);
 
 /*
+ * mla_decode_noalloc - mla_decode_plan (algo QKVP_ALGO_AUTO) followed by mla_decode_run, for callers
+ * that cannot allocate device memory: a serving loop that has already given every free byte of the
+ * GPU to a pre-sized KV pool, or a latency-critical decode step that must not risk the device-wide
+ * synchronisation an allocation can bring. The source pages have no counterpart for this call.
+ *
+ * The work table and the split partials live in one fixed device array of
+ * QKVP_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library holds until
+ * the process exits. The call allocates nothing (no cudaMalloc or cudaFree, no allocating library
+ * routine, no host heap). Problems that do not fit return QKVP_E_WORKSPACE before any device work:
+ * more than QKVP_NOALLOC_MAX_BATCH requests, more than QKVP_NOALLOC_MAX_SEGMENTS segments, or a
+ * table plus partials above the array size (at 128 heads, about 250 split partials).
+ *
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make this first call before any stream capture. Every call shares the one
+ * array and leaves its partials there; calls whose GPU work overlaps (different streams or host
+ * threads) race on it, so the caller must serialise them. Nothing in the array needs to start at
+ * zero: each call uploads its own table and writes every partial before reading it.
+ * Arguments as for mla_decode_plan and mla_decode_run (page size 64).
+ */
+#define QKVP_NOALLOC_SCRATCH_BYTES (64ull << 20)
+#define QKVP_NOALLOC_MAX_BATCH 8192
+#define QKVP_NOALLOC_MAX_SEGMENTS 16384
+int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int32_t batch,
+                       int32_t num_heads, int32_t kv_dtype, int32_t num_sms, int32_t min_splits,
+                       const void* q, const void* kv_data, const uint8_t* kv_scale,
+                       int64_t num_pages, const int32_t* kv_indices, float sm_scale,
+                       float global_scale, void* out, float* lse, qkvp_stream_t stream);
+
+/*
  * kv_pool_cast_bf16 - the cast-then-attend baseline's pool-wide cast: every E4M3 byte of an FP8
  * pool to its BF16 value (exact; NaN bytes 0x7F/0xFF become 0x7FC0). Source: "The Smoking Gun",
  * section "The Investigation Leading to This Message" (k_buffer = pool.to(q.dtype) over the whole

@@ -23,7 +23,7 @@ ALGO_AUTO, ALGO_MMA_SYNC, ALGO_TCGEN05 = 0, 1, 2
 LATENT_DIM, V_DIM, PAGE_SIZE = 576, 512, 64
 
 EXPORTS = ["kv_append_quant", "mla_decode_plan", "mla_decode_run", "mla_decode_attend",
-           "mla_decode_combine", "kv_pool_cast_bf16",
+           "mla_decode_combine", "mla_decode_noalloc", "kv_pool_cast_bf16",
            "qkvp_encode_f32", "qkvp_status_string", "qkvp_version"]
 
 
@@ -70,12 +70,14 @@ def load(path: str | None = None):
                                      vp, u64, vp]
         L.mla_decode_attend.argtypes = L.mla_decode_run.argtypes
         L.mla_decode_combine.argtypes = [c.POINTER(qkvp_plan), f32, vp, vp, vp, u64, vp]
+        L.mla_decode_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64, vp, f32,
+                                         f32, vp, vp, vp]
         L.kv_pool_cast_bf16.argtypes = [vp, i64, vp, vp]
         L.qkvp_encode_f32.argtypes = [vp, i64, i32, vp, vp]
         L.qkvp_status_string.restype = c.c_char_p
         L.qkvp_status_string.argtypes = [c.c_int]
         for fn in ("kv_append_quant", "mla_decode_plan", "mla_decode_run", "mla_decode_attend",
-                   "mla_decode_combine", "kv_pool_cast_bf16",
+                   "mla_decode_combine", "mla_decode_noalloc", "kv_pool_cast_bf16",
                    "qkvp_encode_f32", "qkvp_version"):
             getattr(L, fn).restype = c.c_int
         _lib = L
@@ -170,6 +172,21 @@ def mla_decode_combine(plan: qkvp_plan, global_scale: float, out, lse, workspace
     st = load().mla_decode_combine(ctypes.byref(plan), float(global_scale), _ptr(out), _ptr(lse),
                                    _ptr(workspace), nbytes, _stream(stream))
     return _check("mla_decode_combine", st, raise_on_error)
+
+
+def mla_decode_noalloc(kv_indptr, kv_len, num_heads: int, kv_dtype: int, q, kv_data, kv_scale,
+                       num_pages: int, kv_indices, sm_scale: float, global_scale: float, out, lse,
+                       num_sms: int = 0, min_splits: int = 0, stream=None,
+                       raise_on_error: bool = True) -> int:
+    """Plan + decode with the library's fixed scratch array, for callers that cannot allocate
+    device memory (see qkvp.h for the size limit and the sharing rules)."""
+    indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
+    lens = np.ascontiguousarray(kv_len, dtype=np.int32)
+    st = load().mla_decode_noalloc(indptr.ctypes.data, lens.ctypes.data, int(lens.shape[0]), num_heads,
+                                   kv_dtype, num_sms, min_splits, _ptr(q), _ptr(kv_data),
+                                   _ptr(kv_scale), int(num_pages), _ptr(kv_indices), float(sm_scale),
+                                   float(global_scale), _ptr(out), _ptr(lse), _stream(stream))
+    return _check("mla_decode_noalloc", st, raise_on_error)
 
 
 def kv_pool_cast_bf16(src, out, stream=None, raise_on_error: bool = True) -> int:

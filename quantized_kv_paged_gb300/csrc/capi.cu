@@ -15,24 +15,9 @@ using namespace qkvp;
 
 namespace {
 
-constexpr uint64_t kAlign = 256;
-
-uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+constexpr uint64_t kAlign = kTableAlign;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-struct TableLayout {
-  uint64_t segs, wptr, rptr, bytes;
-};
-
-TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch) {
-  TableLayout t;
-  t.segs = 0;
-  t.wptr = align_up(static_cast<uint64_t>(segments) * sizeof(Segment));
-  t.rptr = t.wptr + align_up(static_cast<uint64_t>(workers + 1) * 4);
-  t.bytes = t.rptr + align_up(static_cast<uint64_t>(batch + 1) * 4);
-  return t;
-}
 
 int query_sms() {
   int dev = 0, sms = 0;

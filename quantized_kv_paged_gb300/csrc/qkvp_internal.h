@@ -51,6 +51,24 @@ struct DecodeArgs {
   float out_scale;            // g
 };
 
+// Workspace layout of a plan: the segment table, the per-worker segment ranges and the
+// per-request segment ranges, each 256-byte aligned, followed by the FP32 partials.
+constexpr uint64_t kTableAlign = 256;
+inline uint64_t align_up(uint64_t x) { return (x + kTableAlign - 1) / kTableAlign * kTableAlign; }
+
+struct TableLayout {
+  uint64_t segs, wptr, rptr, bytes;
+};
+
+inline TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch) {
+  TableLayout t;
+  t.segs = 0;
+  t.wptr = align_up(static_cast<uint64_t>(segments) * sizeof(Segment));
+  t.rptr = t.wptr + align_up(static_cast<uint64_t>(workers + 1) * 4);
+  t.bytes = t.rptr + align_up(static_cast<uint64_t>(batch + 1) * 4);
+  return t;
+}
+
 cudaError_t launch_append(const void* src, int src_dtype, int64_t n, const int64_t* slots,
                           void* kv_data, uint8_t* kv_scale, int kv_dtype, float g,
                           int64_t num_slots, cudaStream_t s);
