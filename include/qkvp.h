@@ -94,6 +94,9 @@ typedef struct {
   uint64_t table_bytes;      /* bytes of the work table at the start of the workspace */
   uint64_t partial_o_offset; /* byte offset of the FP32 partial outputs in the workspace */
   uint64_t partial_lse_offset;
+  uint64_t status_offset;    /* int32 device status word in the workspace: 0 after planning; a
+                                decode kernel that gave up waiting on its own pipeline (a bug, never
+                                expected) sets bits in it, and its outputs are then undefined */
   uint64_t magic;            /* set by a successful plan; checked by run */
 } qkvp_plan;
 

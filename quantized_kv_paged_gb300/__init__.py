@@ -35,7 +35,7 @@ class qkvp_plan(ctypes.Structure):
         ("total_pages", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64), ("table_bytes", ctypes.c_uint64),
         ("partial_o_offset", ctypes.c_uint64), ("partial_lse_offset", ctypes.c_uint64),
-        ("magic", ctypes.c_uint64)]
+        ("status_offset", ctypes.c_uint64), ("magic", ctypes.c_uint64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

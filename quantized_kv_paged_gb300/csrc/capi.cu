@@ -154,21 +154,34 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16)
     return QKVP_E_UNSUPPORTED;
   if (algo == QKVP_ALGO_AUTO) algo = QKVP_ALGO_MMA_SYNC;
-  if (algo != QKVP_ALGO_MMA_SYNC) return QKVP_E_UNSUPPORTED;
+  if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05) return QKVP_E_UNSUPPORTED;
+  if (algo == QKVP_ALGO_TCGEN05 && num_heads != 128) return QKVP_E_UNSUPPORTED;
   if (batch > 0 && kv_indptr_host[0] != 0) return QKVP_E_INVALID;
   for (int r = 0; r < batch; ++r) {
     const int64_t np = static_cast<int64_t>(kv_indptr_host[r + 1]) - kv_indptr_host[r];
     if (np < 0 || kv_len_host[r] < 0) return QKVP_E_INVALID;
     if ((static_cast<int64_t>(kv_len_host[r]) + page_size - 1) / page_size > np) return QKVP_E_INVALID;
   }
-  if (num_sms <= 0) {
-    num_sms = query_sms();
-    if (num_sms <= 0) return QKVP_E_CUDA;
+  int cpw, workers;
+  if (algo == QKVP_ALGO_TCGEN05) {
+    // one worker = one CTA pair; by default as many pairs as the device runs at once
+    cpw = 2;
+    if (num_sms <= 0) {
+      workers = tc_max_active_clusters();
+      if (workers <= 0) return QKVP_E_CUDA;
+    } else {
+      workers = std::max(1, num_sms / 2);
+    }
+  } else {
+    if (num_sms <= 0) {
+      num_sms = query_sms();
+      if (num_sms <= 0) return QKVP_E_CUDA;
+    }
+    const int hc = mma_heads_per_cta(num_heads);
+    if (hc == 0) return QKVP_E_UNSUPPORTED;
+    cpw = num_heads / hc;
+    workers = std::max(1, num_sms / cpw);
   }
-  const int hc = mma_heads_per_cta(num_heads);
-  if (hc == 0) return QKVP_E_UNSUPPORTED;
-  const int cpw = num_heads / hc;
-  const int workers = std::max(1, num_sms / cpw);
 
   Split s;
   split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, s);
@@ -189,6 +202,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   plan->total_pages = s.total_pages;
   plan->total_tokens = s.total_tokens;
   plan->table_bytes = t.bytes;
+  plan->status_offset = t.status;
   plan->partial_o_offset = t.bytes;
   plan->partial_lse_offset = t.bytes + align_up(static_cast<uint64_t>(s.partials) * num_heads * QKVP_V_DIM * 4);
   plan->workspace_bytes = plan->partial_lse_offset + align_up(static_cast<uint64_t>(s.partials) * num_heads * 4);
@@ -241,6 +255,7 @@ DecodeArgs make_args(const qkvp_plan* plan, const void* q, const void* kv_data, 
   a.req_seg_ptr = reinterpret_cast<const int32_t*>(ws + t.rptr);
   a.part_o = reinterpret_cast<float*>(ws + plan->partial_o_offset);
   a.part_lse = reinterpret_cast<float*>(ws + plan->partial_lse_offset);
+  a.status = reinterpret_cast<int*>(ws + t.status);
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.batch = plan->batch;
@@ -268,7 +283,8 @@ int mla_decode_attend(const qkvp_plan* plan, const void* q, const void* kv_data,
   if (plan->kv_dtype == QKVP_KV_NVFP4 && (!kv_scale || !aligned(kv_scale, 16))) return QKVP_E_INVALID;
   const DecodeArgs a = make_args(plan, q, kv_data, kv_scale, num_pages, kv_indices, sm_scale,
                                  global_scale, out, lse, workspace);
-  cudaError_t e = launch_decode_mma(a, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = plan->algo == QKVP_ALGO_TCGEN05 ? launch_decode_tc(a, st_) : launch_decode_mma(a, st_);
   return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
 }
 

@@ -152,6 +152,7 @@ extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* 
   plan.num_workers = workers;
   plan.ctas_per_worker = cpw;
   plan.table_bytes = t.bytes;
+  plan.status_offset = t.status;
   plan.partial_o_offset = t.bytes;
   plan.partial_lse_offset = t.bytes + align_up(static_cast<uint64_t>(plan.num_partials) * num_heads * kDv * 4);
   plan.workspace_bytes = plan.partial_lse_offset + align_up(static_cast<uint64_t>(plan.num_partials) * num_heads * 4);

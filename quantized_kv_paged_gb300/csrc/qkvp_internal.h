@@ -46,6 +46,7 @@ struct DecodeArgs {
   float* part_lse;            // [num_segments][H], log2 domain
   uint16_t* out;              // bf16 [B][H][512]
   float* lse;                 // [B][H] natural log, may be null
+  int* status;                // device status word (timeouts), inside the workspace
   int batch, heads, num_workers, ctas_per_worker, num_segments, kv_dtype;
   float scale_log2;           // sm_scale * g * log2(e)
   float out_scale;            // g
@@ -56,8 +57,9 @@ struct DecodeArgs {
 constexpr uint64_t kTableAlign = 256;
 inline uint64_t align_up(uint64_t x) { return (x + kTableAlign - 1) / kTableAlign * kTableAlign; }
 
+// The status word is zero after planning; a kernel that gives up waiting sets bits in it.
 struct TableLayout {
-  uint64_t segs, wptr, rptr, bytes;
+  uint64_t segs, wptr, rptr, status, bytes;
 };
 
 inline TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch) {
@@ -65,7 +67,8 @@ inline TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch
   t.segs = 0;
   t.wptr = align_up(static_cast<uint64_t>(segments) * sizeof(Segment));
   t.rptr = t.wptr + align_up(static_cast<uint64_t>(workers + 1) * 4);
-  t.bytes = t.rptr + align_up(static_cast<uint64_t>(batch + 1) * 4);
+  t.status = t.rptr + align_up(static_cast<uint64_t>(batch + 1) * 4);
+  t.bytes = t.status + kTableAlign;
   return t;
 }
 
@@ -80,5 +83,7 @@ cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
 
 // Heads per CTA of the mma.sync kernel for a head count (0 if unsupported).
 int mma_heads_per_cta(int heads);
+// CTA pairs of the tcgen05 kernel that the current device runs at once (-1 on error).
+int tc_max_active_clusters();
 
 }  // namespace qkvp

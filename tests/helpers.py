@@ -63,6 +63,8 @@ def gpu_decode(w: synth.Workload, kv: int, pools, g: float = 1.0, num_sms: int =
     idx = torch.from_numpy(w.kv_indices if indices is None else indices).to(dev)
     q.mla_decode_run(plan, w.q, pools[0], pools[1], w.num_pages, idx, w.sm_scale, g, out, lse, ws)
     torch.cuda.synchronize()
+    status = int(ws[plan.status_offset:plan.status_offset + 4].view(torch.int32).item())
+    assert status == 0, f"decode kernel gave up waiting (status {status:#x})"
     return out, lse, plan
 
 

@@ -18,7 +18,7 @@ FP8, NVFP4, BF16 = q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_BF16
 
 
 def _run(w, kv, g=1.0, raw=False, **kw):
-    out, lse, plan = gpu_decode(w, kv, gpu_pools(w, kv, g), g, **kw)
+    out, lse, plan = gpu_decode(w, kv, gpu_pools(w, kv, g), g, algo=q.ALGO_MMA_SYNC, **kw)
     o_ref, lse_ref = oracle_decode(w, kv, oracle_pools(w, kv, g), g, lens=kw.get("lens"))
     stats = compare(out.float().cpu().numpy().reshape(-1, 512), lse.cpu().numpy().reshape(-1),
                     o_ref, lse_ref, raw=raw)
@@ -53,7 +53,7 @@ def test_min_splits_and_single_request(qkvp):
 def test_all_requests_empty(qkvp):
     w = synth.build_workload("empty", [0, 0], heads=16, pool_pages=2, seed=2, device="cuda",
                              extra_pages=[1, 0])
-    out, lse, plan = gpu_decode(w, FP8, gpu_pools(w, FP8))
+    out, lse, plan = gpu_decode(w, FP8, gpu_pools(w, FP8), algo=q.ALGO_MMA_SYNC)
     assert torch.all(out == 0) and torch.all(torch.isinf(lse)) and torch.all(lse < 0)
 
 
@@ -61,7 +61,7 @@ def test_bad_page_ids_are_masked_not_read(qkvp):
     w = synth.build_workload("bad", [130, 70], heads=16, pool_pages=6, seed=4, device="cuda")
     idx = w.kv_indices.copy()
     idx[1] = 1 << 30          # second page of request 0 lies outside the pool
-    out, lse, _ = gpu_decode(w, FP8, gpu_pools(w, FP8), indices=idx)
+    out, lse, _ = gpu_decode(w, FP8, gpu_pools(w, FP8), indices=idx, algo=q.ALGO_MMA_SYNC)
     assert torch.all(torch.isfinite(out.float()))
     # request 0 then attends only its first page and its last two tokens; request 1 is untouched
     w0 = synth.build_workload("bad", [130, 70], heads=16, pool_pages=6, seed=4, device="cpu")
@@ -75,7 +75,7 @@ def test_subnormal_latents_survive_dequant(qkvp):
     codes = torch.randint(1, 8, (w.num_pages, 64, 576), dtype=torch.uint8, device="cuda")
     sign = torch.randint(0, 2, codes.shape, dtype=torch.uint8, device="cuda") << 7
     w.pool_fp8.copy_(codes | sign)
-    out, lse, _ = gpu_decode(w, FP8, (w.pool_fp8, None))
+    out, lse, _ = gpu_decode(w, FP8, (w.pool_fp8, None), algo=q.ALGO_MMA_SYNC)
     o_ref, lse_ref = oracle_decode(w, FP8, (w.pool_fp8.cpu().numpy(), None))
     got = out.float().cpu().numpy().reshape(-1, 512)
     assert np.abs(o_ref).max() > 1e-4
@@ -98,7 +98,7 @@ def _sample_pairs(w, n, seed):
     return np.stack([r, h], 1).astype(np.int32)
 
 
-def _full_check(name, kv, g_mode="one", n_pairs=12, append=False):
+def _full_check(name, kv, g_mode="one", n_pairs=12, append=False, algo=0):
     w = synth.workload(name, device="cuda")
     if g_mode == "calibrated":
         amax = float(w.src_fp8.view(torch.float8_e4m3fn).float().abs().max())
@@ -118,7 +118,7 @@ def _full_check(name, kv, g_mode="one", n_pairs=12, append=False):
     if kv == NVFP4:
         assert np.array_equal(pools[0].cpu().numpy(), host[0]) and np.array_equal(pools[1].cpu().numpy(), host[1])
     min_splits = 148 if w.batch == 1 else 0
-    out, lse, plan = gpu_decode(w, kv, pools, g, min_splits=min_splits, lens=lens)
+    out, lse, plan = gpu_decode(w, kv, pools, g, min_splits=min_splits, lens=lens, algo=algo)
     assert torch.all(torch.isfinite(out.float())) and torch.all(torch.isfinite(lse))
     pairs = _sample_pairs(w, n_pairs, 7)
     o_ref, lse_ref = oracle_decode(w, kv, host, g, pairs=pairs, lens=lens)
@@ -130,19 +130,19 @@ def _full_check(name, kv, g_mode="one", n_pairs=12, append=False):
 
 
 def test_full_fp8_b44_l32k(qkvp):
-    _full_check("mla_fp8_b44_h128_l32k", FP8)
+    _full_check("mla_fp8_b44_h128_l32k", FP8, algo=q.ALGO_MMA_SYNC)
 
 
 def test_full_nvfp4_b10_l160k_with_append(qkvp):
-    _full_check("mla_nvfp4_b10_h128_l160k", NVFP4, append=True, n_pairs=8)
+    _full_check("mla_nvfp4_b10_h128_l160k", NVFP4, append=True, n_pairs=8, algo=q.ALGO_MMA_SYNC)
 
 
 @pytest.mark.parametrize("g_mode", ["one", "calibrated"])
 def test_full_nvfp4_b1_l1m(qkvp, g_mode):
-    plan = _full_check("mla_nvfp4_b1_h128_l1m", NVFP4, g_mode=g_mode, n_pairs=6)
+    plan = _full_check("mla_nvfp4_b1_h128_l1m", NVFP4, g_mode=g_mode, n_pairs=6, algo=q.ALGO_MMA_SYNC)
     assert plan.num_segments >= 148
 
 
 @pytest.mark.parametrize("kv", [FP8, BF16])
 def test_full_mixed_pool(qkvp, kv):
-    _full_check("mla_fp8_mixed_b64_h128_pool495552", kv, n_pairs=16)
+    _full_check("mla_fp8_mixed_b64_h128_pool495552", kv, n_pairs=16, algo=q.ALGO_MMA_SYNC)
