@@ -31,6 +31,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_local, uint32_t
                :: "r"(bar_local), "r"(rank) : "memory");
 }
 
+// Relaxed remote arrive: no ordering of this thread's earlier memory operations (use only when
+// the operations it signals are already complete, e.g. loads whose values have been used).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_local, uint32_t rank) {
+  asm volatile("{\n\t.reg .b32 ra;\n\t"
+               "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+               "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [ra];\n\t}"
+               :: "r"(bar_local), "r"(rank) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
@@ -74,6 +83,12 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
 
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void cluster_sync() {
