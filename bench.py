@@ -377,7 +377,8 @@ def main():
     value = world * pb.kv_bytes / (ms_max * 1e-3) / 1e9
     main_stats = summarize(pb, ms, attend_ms, pk)
     attend_s = attend_ms * 1e-3
-    roof = {"bound": "tensor", "kernel": "decode_mma_kernel (split-KV attend)",
+    kname = "decode_tc_kernel (tcgen05 CTA-pair split-KV attend)" if pb.plan.algo == 2 else "decode_mma_kernel (split-KV attend)"
+    roof = {"bound": "tensor", "kernel": kname,
             "achieved": round(pb.flops / attend_s / 1e12, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(pb.flops / attend_s / 1e12 / pk["bf16_tflops"], 4),
             "traffic": profiled_traffic(MAIN),

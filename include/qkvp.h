@@ -66,8 +66,8 @@ typedef enum { QKVP_SRC_FP8_E4M3 = 1, QKVP_SRC_BF16 = 2 } qkvp_src_dtype;
 /* Decode kernel families. AUTO lets the planner choose. */
 typedef enum {
   QKVP_ALGO_AUTO = 0,
-  QKVP_ALGO_MMA_SYNC = 1,  /* warp-level mma.sync BF16 split-KV kernel */
-  QKVP_ALGO_TCGEN05 = 2    /* tcgen05/TMEM CTA-pair split-KV kernel */
+  QKVP_ALGO_MMA_SYNC = 1,  /* warp-level mma.sync split-KV kernel, any supported head count */
+  QKVP_ALGO_TCGEN05 = 2    /* tcgen05/TMEM CTA-pair split-KV kernel, 128 heads (AUTO picks it) */
 } qkvp_algo;
 
 #define QKVP_LATENT_DIM 576
@@ -201,7 +201,7 @@ int mla_decode_combine(const qkvp_plan* plan, float global_scale, void* out, flo
                        void* workspace, uint64_t workspace_bytes, qkvp_stream_t stream);
 
 /*
- * mla_decode_noalloc - mla_decode_plan (algo QKVP_ALGO_AUTO) followed by mla_decode_run, for callers
+ * mla_decode_noalloc - mla_decode_plan (algo QKVP_ALGO_MMA_SYNC) followed by mla_decode_run, for callers
  * that cannot allocate device memory: a serving loop that has already given every free byte of the
  * GPU to a pre-sized KV pool, or a latency-critical decode step that must not risk the device-wide
  * synchronisation an allocation can bring. The source pages have no counterpart for this call.

@@ -153,7 +153,8 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   if (num_heads < 16 || num_heads > 128 || num_heads % 16) return QKVP_E_UNSUPPORTED;
   if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16)
     return QKVP_E_UNSUPPORTED;
-  if (algo == QKVP_ALGO_AUTO) algo = QKVP_ALGO_MMA_SYNC;
+  // the tcgen05 CTA-pair kernel needs exactly 128 heads; other head counts use the mma.sync kernel
+  if (algo == QKVP_ALGO_AUTO) algo = num_heads == 128 ? QKVP_ALGO_TCGEN05 : QKVP_ALGO_MMA_SYNC;
   if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05) return QKVP_E_UNSUPPORTED;
   if (algo == QKVP_ALGO_TCGEN05 && num_heads != 128) return QKVP_E_UNSUPPORTED;
   if (batch > 0 && kv_indptr_host[0] != 0) return QKVP_E_INVALID;

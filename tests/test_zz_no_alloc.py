@@ -36,7 +36,8 @@ def test_noalloc_matches_plan_and_run_two_calls_in_a_row(cuda_device):
         w = synth.build_workload("noalloc", lens, heads=heads, pool_pages=200, seed=heads + len(lens),
                                  outliers=4, device="cuda")
         pools = gpu_pools(w, kv, g)
-        ref_out, ref_lse, plan = gpu_decode(w, kv, pools, g, num_sms=sms)
+        # the same kernel family as the no-allocation call, so both plans split the work alike
+        ref_out, ref_lse, plan = gpu_decode(w, kv, pools, g, num_sms=sms, algo=q.ALGO_MMA_SYNC)
         assert plan.num_split_requests > 0        # the scratch partials are exercised
         out, lse = _noalloc(w, kv, pools, g, sms)
         compare(out.float().cpu().numpy().reshape(-1, 512), lse.cpu().numpy().reshape(-1),
