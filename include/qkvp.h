@@ -20,14 +20,16 @@
  * Memory layout (all device buffers are caller-owned; the library allocates no device memory and
  * keeps no global mutable state):
  *  - slot s = page * page_size + offset; page_size must be 64.
- *  - FP8 pool  : kv_data uint8 [num_pages][64][576], one E4M3 byte per latent element.
+ *  - FP8 pool  : kv_data uint8 [num_pages][64][576], one E4M3 byte per latent element. The decode
+ *                entry points read kv_data (any pool type) with 32-byte loads: it must be 32-byte aligned.
  *  - NVFP4 pool: kv_data uint8 [num_pages][64][288] packed E2M1 pairs (element 2k in the low nibble
  *                of byte k, 2k+1 in the high nibble) and kv_scale uint8 [num_pages][64][36] E4M3
  *                block scales (block j covers elements 16j..16j+15). 324 bytes per token = 9/16 of
  *                FP8. An element decodes to global_scale * scale(block) * e2m1(code).
  *  - BF16 pool : kv_data uint16 [num_pages][64][576] (the cast-then-attend baseline only).
  *  - q         : bf16 [batch][num_heads][576], row-major, contiguous.
- *  - out       : bf16 [batch][num_heads][512]; lse: float [batch][num_heads] (natural log), or NULL.
+ *  - out       : bf16 [batch][num_heads][512], 16-byte aligned (the attend kernels store 16-byte
+ *                vectors); lse: float [batch][num_heads] (natural log), or NULL.
  *
  * Errors: every call returns an int status (qkvp_status). Arguments are checked before anything is
  * launched; a failed check launches nothing. QKVP_E_CUDA reports a CUDA error from a launch or copy

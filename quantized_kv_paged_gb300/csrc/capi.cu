@@ -279,8 +279,8 @@ int mla_decode_attend(const qkvp_plan* plan, const void* q, const void* kv_data,
   int st = check_run_args(plan, num_pages, sm_scale, global_scale, workspace, workspace_bytes);
   if (st != QKVP_OK) return st;
   if (plan->batch == 0 || plan->num_segments == 0) return QKVP_OK;
-  if (!q || !out || !aligned(q, 16) || !aligned(out, 4) || (lse && !aligned(lse, 4))) return QKVP_E_INVALID;
-  if (!kv_data || !kv_indices || !aligned(kv_data, 16) || !aligned(kv_indices, 4)) return QKVP_E_INVALID;
+  if (!q || !out || !aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return QKVP_E_INVALID;
+  if (!kv_data || !kv_indices || !aligned(kv_data, 32) || !aligned(kv_indices, 4)) return QKVP_E_INVALID;
   if (plan->kv_dtype == QKVP_KV_NVFP4 && (!kv_scale || !aligned(kv_scale, 16))) return QKVP_E_INVALID;
   const DecodeArgs a = make_args(plan, q, kv_data, kv_scale, num_pages, kv_indices, sm_scale,
                                  global_scale, out, lse, workspace);

@@ -8,29 +8,38 @@
 // probabilities), the same arithmetic as the mma.sync kernel.
 //
 // Work split. The FP32 output of 128 heads x 512 dims fills all 512 TMEM columns of an SM, so one
-// work item runs on a pair of CTAs (a cluster of two). CTA c owns latent dims [256c, 256c + 256) of
-// the 512 "nope" dims and [512 + 32c, 512 + 32c + 32) of the rope dims: it computes the partial
-// logits over its 288 dims, trades them with its peer through distributed shared memory, and both
-// CTAs add the two partials in the same order, so they hold bit-identical logits, maxima and
-// probabilities. Each then accumulates its own 256 output dims. Dequantization is never duplicated.
+// work item runs on a pair of CTAs (a cluster of two), and the pair splits each 64-token page by
+// tokens: CTA c computes the full 576-dim logits of tokens [32c, 32c + 32) for all 128 heads, the
+// two CTAs trade their 128 row maxima (512 bytes) so that both scale by the same running maximum,
+// and each sends its half of the probabilities P (128 x 32 FP16, 8 KB) to the other with one bulk
+// asynchronous copy. CTA c then accumulates output dims [256c, 256c + 256) over all 64 tokens: the
+// V rows of its own tokens are already in its operand tile, and it dequantizes the other 32 tokens'
+// rows for its 256 dims itself (a second read of those bytes, served by L2). Trading logits
+// instead (a split by dims) would move 32 KB per page over the SM-to-SM network, whose bandwidth
+// (about 12 bytes per clock per SM) then bounds the whole kernel.
 //
-// Per CTA (256 threads, two warps per SM sub-partition):
-//   warps 0-3 (softmax): thread h owns head h = TMEM lane h. Loads Q once per request (the nope half
-//     into TMEM as the A operand of Q.K^T, the rope half into shared memory), then per page: reads
-//     its 64 partial logits from TMEM, exchanges them, runs the FP32 online softmax (base 2, with a
-//     lazy rescale of O when the running maximum grows by more than 2^8), and writes its row of
-//     P (FP16) to shared memory. At the end of a segment it reads O from TMEM and writes the output.
-//   warps 4-6 (dequant): per page, load this CTA's half of the raw page from global memory (the next
-//     page's loads are in flight while the current one is converted), convert to FP16 and write the
-//     swizzled operand tile (three tiles in a ring).
-//   warp 7 (MMA): one thread issues S = Q.K^T (M 128 heads x N 64 tokens x K 288) into one of two
-//     TMEM logit buffers and O += P.V (M 128 x N 256 x K 64) into the TMEM accumulator; tcgen05.commit
-//     signals the other roles through mbarriers.
-// TMEM: O [0, 256), Q nope [256, 384), logits [384, 448) and [448, 512).
+// Per CTA (384 threads, three warps per SM sub-partition):
+//   warps 0-3 (softmax): thread h owns head h = TMEM lane h. Loads Q once per request (in this CTA's
+//     contraction order: the first 384 dims into TMEM as the A operand of Q.K^T, the rest into
+//     shared memory), then per page:
+//     reads its 32 logits, trades the row maximum with the peer (asynchronous remote stores counted
+//     on the peer's mbarrier, so no fence is needed), runs the FP32 online softmax (base
+//     2, lazy rescale of O when the running maximum grows by more than 2^8), writes its row of P and
+//     hands the half to the peer. At the end of a segment the two CTAs trade their row sums, and
+//     each writes its 256 output dims.
+//   warps 4-8 (dequant): per page, load the raw bytes of the own 32 tokens (all dims) and of the
+//     other 32 tokens (own V dims), the next page's loads in flight while the current page is
+//     converted, and write FP16 operand tiles (two rings, split by how long each part is read).
+//   warps 11 and 9 (QK): one thread each issues S = Q.K^T (M 128 heads x N 32 tokens x K 576) into
+//     TMEM for the even / odd pages (the two logit buffers).
+//   warp 10 (PV): one thread issues O += P.V (M 128 x N 256 x K 64) into the TMEM accumulator; the
+//     P.V commit that frees a P buffer goes to both CTAs. tcgen05.commit signals the other roles.
+// TMEM: O [0, 256), Q dims 0..383 as FP16 pairs [256, 448), two logit buffers [448, 512).
 // Barrier phases: every barrier is waited on by parity, which is only sound while the barrier is at
-// most one phase away from the phase waited for. Buffers indexed by the global page counter g keep
-// that true; the PV-completion barrier is split by the parity of g because the softmax warps wait on
-// it only now and then (lazy rescales, segment ends), and QK(g) completing implies PV(g - 2) has.
+// most one phase away from the phase waited for; the comments at each wait say why that holds. A
+// barrier whose waiter skips phases (a Q.K^T thread sees only every other page) would break that, so
+// the Q.K^T threads wait only on their own K slot (one slot per parity, armed after both rings of the
+// page are written), and the new-request Q is published as a counter instead of a barrier phase.
 // Every wait is bounded; a timeout sets bits in the status word and the CTA drains and exits.
 #include <cstdint>
 
@@ -41,33 +50,52 @@
 namespace qkvp {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kDQ = 96;                     // dequant threads (warps 4-6)
-constexpr int kTiles = 3;
-constexpr uint32_t kTileBytes = 36864;      // nope 64 tokens x 256 dims (32 KB) + rope 64 x 32 (4 KB)
-constexpr uint32_t kRopeOff = 32768;
-constexpr uint32_t kPBytes = 16384;         // 128 heads x 64 tokens FP16
-constexpr uint32_t kQRBytes = 8192;         // 128 heads x 32 rope dims FP16
-constexpr uint32_t kXBytes = 32768;         // 128 heads x 64 FP32 logits, [16-byte chunk][head]
+constexpr int kThreads = 384;
+constexpr int kDQ = 160;                     // dequant threads (warps 4-8)
+// MMA issue: one thread in each of warps 9 and 11 issues Q.K^T for odd / even pages, one in warp 10
+// issues P.V. A thread waits a few tens of cycles after each tcgen05.mma it issues before the next one
+// can go; several issuing threads overlap those waits and keep the tensor pipe fed.
+constexpr int kQkWarpOdd = 9, kPvWarp = 10, kMmaWarp = 11;
+constexpr int kHalf = 32;                    // tokens of a page per CTA
+constexpr uint32_t kAtom = 4096;             // 32 token rows x 64 dims FP16, 128-byte swizzle
+// Operand tiles of a page live in two rings by lifetime: the K-only ring holds the own tokens' dims
+// that only Q.K^T reads (the other CTA's 256 nope dims and the 64 rope dims: 5 atoms), freed when
+// Q.K^T completes; the V ring holds this CTA's 256 V dims of the own tokens (read by Q.K^T and P.V)
+// and of the other 32 tokens (P.V only): 8 atoms, freed when P.V completes.
+constexpr int kKSlots = 2, kVSlots = 3;
+constexpr uint32_t kKSlot = 5 * kAtom;
+constexpr uint32_t kVSlot = 8 * kAtom;
+constexpr uint32_t kPHalf = 8192;            // 128 heads x 32 tokens FP16, 64-byte swizzle
+constexpr uint32_t kPBytes = 2 * kPHalf;
+constexpr uint32_t kQAtom = 16384;           // 128 heads x 64 dims FP16, 128-byte swizzle
+constexpr int kQTmemDims = 384;              // Q dims held in TMEM; dims 384..575 in shared memory
+constexpr int kQSmemAtoms = (kLatent - kQTmemDims) / 64;
 
-constexpr uint32_t OFF_TILE = 0;
-constexpr uint32_t OFF_P = OFF_TILE + kTiles * kTileBytes;
-constexpr uint32_t OFF_QR = OFF_P + 2 * kPBytes;
-constexpr uint32_t OFF_X = OFF_QR + kQRBytes;
-constexpr uint32_t OFF_BAR = OFF_X + 2 * kXBytes;
+constexpr uint32_t OFF_K = 0;
+constexpr uint32_t OFF_V = OFF_K + kKSlots * kKSlot;
+constexpr uint32_t OFF_P = OFF_V + kVSlots * kVSlot;
+constexpr uint32_t OFF_Q = OFF_P + 2 * kPBytes;
+constexpr uint32_t OFF_RM = OFF_Q + kQSmemAtoms * kQAtom;   // 2 x 128 FP32: the peer's row maxima
+constexpr uint32_t OFF_LX = OFF_RM + 2 * 512;               // 2 x 128 FP32: the peer's row sums
+constexpr uint32_t OFF_BAR = OFF_LX + 2 * 512;
 enum : uint32_t {
-  B_TILE_FULL = 0, B_TILE_EMPTY = 3, B_S_FULL = 6, B_S_FREE = 8, B_P_FULL = 10, B_P_FREE = 12,
-  B_X_FULL = 14, B_O_DONE = 16, B_Q_READY = 18, B_FINAL = 19, B_X_FREE = 20, NUM_BARS = 22
+  B_K_FULL = 0, B_K_EMPTY = 2, B_V_FULL = 4, B_V_EMPTY = 7, B_S_FULL = 10, B_S_FREE = 12, B_P_LOCAL = 14,
+  B_P_FULL = 16, B_P_FREE = 18, B_O_DONE = 20, B_Q_READY = 22, B_FINAL = 23, B_RM_FULL = 24, B_LX_FULL = 26,
+  NUM_BARS = 28
 };
 constexpr uint32_t OFF_TSLOT = OFF_BAR + 8 * NUM_BARS;
-constexpr uint32_t OFF_QMAX = OFF_TSLOT + 4;
-constexpr uint32_t OFF_ABORT = OFF_QMAX + 4;
-constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
+constexpr uint32_t OFF_ABORT = OFF_TSLOT + 4;
+constexpr uint32_t OFF_QVER = OFF_ABORT + 4;        // number of request Q rows published so far
+constexpr uint32_t kSmemUsed = OFF_QVER + 8;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // slack to align the base to 1024 bytes
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(OFF_V % 1024 == 0 && OFF_P % 1024 == 0 && OFF_Q % 1024 == 0, "swizzle atoms");
 
-constexpr uint32_t TM_O = 0, TM_QN = 256, TM_S = 384;
+// TMEM: O, Q dims 0..383 as FP16 pairs, two logit buffers of 32 columns
+constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 448;
+static_assert(TM_Q + kQTmemDims / 2 == TM_S && TM_S + 2 * kHalf == 512, "TMEM columns");
 
-constexpr uint32_t kIdescQK = tc::idesc_f16(128, 64, 0, 0);
+constexpr uint32_t kIdescQK = tc::idesc_f16(128, kHalf, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_f16(128, 256, 0, 1);
 
 // Walks a worker's (segment, page) sequence.
@@ -93,77 +121,117 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
   return v;
 }
 
+// 32 bytes from global memory through the non-coherent path (the address must be 32-byte aligned).
+__device__ __forceinline__ void ldg_nc32(const void* p, uint32_t (&v)[8]) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(p));
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
-  return v;
+
+// ---- dequantization of a page into the two operand rings -------------------------------------
+// K slot: own tokens (rows 0..31 = tokens 32c..32c+31) x the 4 nope atoms of the other CTA's dims,
+// then the rope atom. V slot: own tokens x this CTA's 4 nope atoms (dims 256c..256c+255), then the
+// other 32 tokens (rows = tokens 32(1-c)..) x the same 4 atoms. Atoms are 64 dims x 32 rows, 4 KB,
+// 128-byte swizzle. Work is cut into items of 16 raw bytes; consecutive items cover the 16-byte
+// chunks of neighbouring rows of one atom so that every group of eight 16-byte shared stores lands
+// in eight distinct bank groups. Rows of tokens past the page's valid count are written as zeros (the
+// pool may hold anything there, NaN codes included).
+struct Item {
+  int tok;          // token within the page
+  int row;          // row within the atom
+  int dim;          // first latent dim of the item
+  bool in_v;        // destination ring
+  uint32_t off;     // byte offset of the item's atom within its slot
+};
+
+__device__ __forceinline__ Item item_at(int own_items, int q, int c, int per_atom, int j, int row) {
+  Item it;
+  const bool own = q < own_items;
+  const int qq = own ? q : q - own_items;
+  const int a = qq / per_atom;              // own: latent atom 0..8; other: V atom 0..3
+  it.row = row;
+  it.tok = own ? kHalf * c + row : kHalf * (1 - c) + row;
+  it.dim = (own ? 0 : 256 * c) + 64 * a + j;
+  if (!own) { it.in_v = true; it.off = (4 + a) * kAtom; }
+  else if (a < 8 && (a >> 2) == c) { it.in_v = true; it.off = (a & 3) * kAtom; }
+  else { it.in_v = false; it.off = (a < 8 ? (a & 3) : 4) * kAtom; }
+  return it;
 }
 
-// ---- dequantization of one page half into an operand tile --------------------------------------
-// Tile layout: nope dims [256c, 256c + 256) as 4 atoms of 64 dims (8 KB each, 128-byte swizzle,
-// rows = tokens); rope dims [512 + 32c, +32) as one 64-byte-swizzle region (rows = tokens).
 template <int KV> struct Dequant;
 
 template <> struct Dequant<KV_FP8> {
-  static constexpr int kIters = 12;         // 64 tokens x 18 chunks of 16 bytes / 96 threads
-  struct Raw { uint4 v[kIters]; };
+  // 32 dims (32 raw bytes, one 32-byte load) per item, 2 items per atom row: own 32 rows x 18, other
+  // 32 rows x 8. Wide loads halve the load instructions, which the per-SM queue of outstanding
+  // global loads otherwise throttles.
+  static constexpr int kOwn = 32 * 18, kItems = kOwn + 32 * 8;
+  static constexpr int kIters = (kItems + kDQ - 1) / kDQ;
+  struct Raw { uint32_t v[kIters][8]; };
+  __device__ static Item at(int q, int c) {
+    const int qq = q < kOwn ? q : q - kOwn;
+    return item_at(kOwn, q, c, 64, 32 * (qq & 1), ((qq >> 3) & 7) * 4 + ((qq >> 1) & 3));
+  }
   __device__ static void load(Raw& r, const DecodeArgs& a, int64_t page, int valid, int c, int t) {
     const uint8_t* base = a.kv + page * (kPage * kLatent);
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
-      const int q = t + kDQ * i, tok = q / 18, k = q % 18;
-      if (tok < valid) r.v[i] = ldg_nc(base + tok * kLatent + (k < 16 ? 256 * c + 16 * k : 512 + 32 * c + 16 * (k - 16)));
+      const int q = t + kDQ * i;
+      const Item it = at(q, c);
+      if (q < kItems && it.tok < valid) ldg_nc32(base + it.tok * kLatent + it.dim, r.v[i]);
     }
   }
-  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int, int t, uint32_t tile) {
+  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int c, int t, uint32_t ks, uint32_t vs) {
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
-      const int q = t + kDQ * i, tok = q / 18, k = q % 18;
-      uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-      if (tok < valid) {
-        const uint4 v = r.v[i];
-        lo = make_uint4(dev::e4m3x2_to_f16x2(v.x & 0xFFFF), dev::e4m3x2_to_f16x2(v.x >> 16),
-                        dev::e4m3x2_to_f16x2(v.y & 0xFFFF), dev::e4m3x2_to_f16x2(v.y >> 16));
-        hi = make_uint4(dev::e4m3x2_to_f16x2(v.z & 0xFFFF), dev::e4m3x2_to_f16x2(v.z >> 16),
-                        dev::e4m3x2_to_f16x2(v.w & 0xFFFF), dev::e4m3x2_to_f16x2(v.w >> 16));
-      }
-      if (k < 16) {
-        const uint32_t at = tile + (k >> 2) * 8192, ch = (k & 3) * 2;
-        sts128(at + tc::sw128_offset(tok, ch), lo);
-        sts128(at + tc::sw128_offset(tok, ch + 1), hi);
-      } else {
-        const uint32_t ch = (k - 16) * 2;
-        sts128(tile + kRopeOff + tc::sw64_offset(tok, ch), lo);
-        sts128(tile + kRopeOff + tc::sw64_offset(tok, ch + 1), hi);
-      }
+      const int q = t + kDQ * i;
+      if (q >= kItems) continue;
+      const Item it = at(q, c);
+      uint32_t o[16];
+#pragma unroll
+      for (int b = 0; b < 16; ++b)
+        o[b] = it.tok < valid ? dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r.v[i][b >> 1] >> (16 * (b & 1)))) : 0u;
+      const uint32_t ch = ((it.dim & 63) >> 3), at = (it.in_v ? vs : ks) + it.off;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        sts128(at + tc::sw128_offset(it.row, ch + u), make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
     }
   }
 };
 
 template <> struct Dequant<KV_NVFP4> {
-  static constexpr int kIters = 6;          // 64 tokens x 9 chunks (8 nope + 1 rope) = 576 / 96
+  // 32 dims (16 packed bytes, two scale blocks) per item, 2 items per atom row
+  static constexpr int kOwn = 32 * 18, kItems = kOwn + 32 * 8;
+  static constexpr int kIters = (kItems + kDQ - 1) / kDQ;
   struct Raw { uint4 v[kIters]; uint32_t s[kIters]; };
+  __device__ static Item at(int q, int c) {
+    const int qq = q < kOwn ? q : q - kOwn;
+    return item_at(kOwn, q, c, 64, 32 * (qq & 1), ((qq >> 3) & 7) * 4 + ((qq >> 1) & 3));
+  }
   __device__ static void load(Raw& r, const DecodeArgs& a, int64_t page, int valid, int c, int t) {
     const uint8_t* base = a.kv + page * (kPage * kPacked);
     const uint8_t* sbase = a.kv_scale + page * (kPage * kScales);
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
-      const int q = t + kDQ * i, tok = q / 9, k = q % 9;
-      if (tok < valid) {
-        r.v[i] = ldg_nc(base + tok * kPacked + (k < 8 ? 128 * c + 16 * k : 256 + 16 * c));
-        r.s[i] = *reinterpret_cast<const uint16_t*>(sbase + tok * kScales + (k < 8 ? 16 * c + 2 * k : 32 + 2 * c));
+      const int q = t + kDQ * i;
+      const Item it = at(q, c);
+      if (q < kItems && it.tok < valid) {
+        r.v[i] = ldg_nc(base + it.tok * kPacked + it.dim / 2);
+        r.s[i] = *reinterpret_cast<const uint16_t*>(sbase + it.tok * kScales + it.dim / 16);
       }
     }
   }
-  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int, int t, uint32_t tile) {
+  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int c, int t, uint32_t ks, uint32_t vs) {
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
-      const int q = t + kDQ * i, tok = q / 9, k = q % 9;
+      const int q = t + kDQ * i;
+      if (q >= kItems) continue;
+      const Item it = at(q, c);
       uint32_t o[16];
-      if (tok < valid) {
+      if (it.tok < valid) {
         const uint32_t sa = r.s[i] & 0xFFu, sb = (r.s[i] >> 8) & 0xFFu;
         const uint32_t ha = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sa | (sa << 8)));
         const uint32_t hb = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
@@ -174,53 +242,50 @@ template <> struct Dequant<KV_NVFP4> {
 #pragma unroll
         for (int b = 0; b < 16; ++b) o[b] = 0;
       }
+      const uint32_t ch = ((it.dim & 63) >> 3), at = (it.in_v ? vs : ks) + it.off;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint4 v = make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
-        if (k < 8) sts128(tile + (k >> 1) * 8192 + tc::sw128_offset(tok, (k & 1) * 4 + u), v);
-        else sts128(tile + kRopeOff + tc::sw64_offset(tok, u), v);
-      }
+      for (int u = 0; u < 4; ++u)
+        sts128(at + tc::sw128_offset(it.row, ch + u), make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
     }
   }
 };
 
 template <> struct Dequant<KV_BF16> {      // the cast-then-attend baseline: BF16 pages
+  // 8 dims (16 bytes) per item, 8 items per atom row; converted in rounds of 12 items per thread
+  static constexpr int kOwn = 32 * 72, kItems = kOwn + 32 * 32;
+  static constexpr int kRound = 12;
   struct Raw {};
+  __device__ static Item at(int q, int c) {
+    const int qq = q < kOwn ? q : q - kOwn;
+    return item_at(kOwn, q, c, 256, 8 * (qq & 7), (qq >> 3) & 31);
+  }
   __device__ static void load(Raw&, const DecodeArgs&, int64_t, int, int, int) {}
-  __device__ static void store(const Raw&, const DecodeArgs& a, int64_t page, int valid, int c, int t, uint32_t tile) {
+  __device__ static void store(const Raw&, const DecodeArgs& a, int64_t page, int valid, int c, int t, uint32_t ks, uint32_t vs) {
     const uint8_t* base = a.kv + page * (kPage * kLatent * 2);
-    // 64 tokens x 36 chunks of 8 BF16 (32 nope + 4 rope) = 2304 chunks / 96 threads, in two halves
+#pragma unroll 1
+    for (int r0 = 0; r0 < kItems; r0 += kDQ * kRound) {
+      uint4 v[kRound];
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      uint4 v[12];
-#pragma unroll
-      for (int i = 0; i < 12; ++i) {
-        const int q = t + kDQ * (12 * h2 + i), tok = q / 36, k = q % 36;
-        if (tok < valid) v[i] = ldg_nc(base + tok * kLatent * 2 + (k < 32 ? (256 * c + 8 * k) : (512 + 32 * c + 8 * (k - 32))) * 2);
+      for (int i = 0; i < kRound; ++i) {
+        const int q = r0 + t + kDQ * i;
+        const Item it = at(q, c);
+        if (q < kItems && it.tok < valid) v[i] = ldg_nc(base + (it.tok * kLatent + it.dim) * 2);
       }
 #pragma unroll
-      for (int i = 0; i < 12; ++i) {
-        const int q = t + kDQ * (12 * h2 + i), tok = q / 36, k = q % 36;
+      for (int i = 0; i < kRound; ++i) {
+        const int q = r0 + t + kDQ * i;
+        if (q >= kItems) continue;
+        const Item it = at(q, c);
         uint4 o = make_uint4(0, 0, 0, 0);
-        if (tok < valid) o = make_uint4(dev::bf16x2_to_f16x2(v[i].x), dev::bf16x2_to_f16x2(v[i].y),
-                                        dev::bf16x2_to_f16x2(v[i].z), dev::bf16x2_to_f16x2(v[i].w));
-        if (k < 32) sts128(tile + (k >> 3) * 8192 + tc::sw128_offset(tok, k & 7), o);
-        else sts128(tile + kRopeOff + tc::sw64_offset(tok, k - 32), o);
+        if (it.tok < valid) o = make_uint4(dev::bf16x2_to_f16x2(v[i].x), dev::bf16x2_to_f16x2(v[i].y),
+                                           dev::bf16x2_to_f16x2(v[i].z), dev::bf16x2_to_f16x2(v[i].w));
+        sts128((it.in_v ? vs : ks) + it.off + tc::sw128_offset(it.row, (it.dim & 63) >> 3), o);
       }
     }
   }
 };
 
 __device__ __forceinline__ bool page_ok(const DecodeArgs& a, int64_t page) { return page >= 0 && page < a.num_pages; }
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-               "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
 
 struct Sync {
   uint32_t bars;
@@ -245,255 +310,181 @@ struct Sync {
   }
 };
 
+// Bounded wait until the counter at `addr` reaches `target` (acquire: what was written before the
+// counter was raised is visible afterwards).
+__device__ bool wait_counter(const Sync& sy, uint32_t addr, uint32_t target) {
+  if (tc::ld_acquire_u32(addr) >= target) return true;
+  const long long t0 = clock64();
+  for (int n = 0;; ++n) {
+    if (tc::ld_acquire_u32(addr) >= target) return true;
+    if ((n & 255) == 0) {
+      if (*sy.abort) return false;
+      if (clock64() - t0 > (1ll << 31)) {
+        *sy.abort = 1;
+        atomicOr(sy.status, 8);
+        return false;
+      }
+    }
+  }
+}
+
 // ---- roles -------------------------------------------------------------------------------------------
 template <int KV>
-__device__ void role_dequant(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, int t, uint32_t tiles) {
+__device__ void role_dequant(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, int t, uint32_t kring,
+                             uint32_t vring) {
   using D = Dequant<KV>;
+  // Page indices are read one page before they are needed (raw loads of page g + 1 are issued while
+  // page g is converted, with the index of page g + 2 already in flight), so no iteration waits on a
+  // dependent index load.
   Cursor cur;
   cur.begin(a, seg_b, seg_e);
-  typename D::Raw raw_cur, raw_nxt;
   if (cur.done()) return;
+  typename D::Raw raw_cur, raw_nxt;
+  Cursor nx = cur;
+  nx.next(a);
   int64_t pg = cur.page(a);
+  int64_t npg = nx.done() ? 0 : nx.page(a);
   int valid = page_ok(a, pg) ? cur.valid() : 0;
   D::load(raw_cur, a, pg, valid, c, t);
   for (int g = 0; !cur.done(); ++g) {
-    Cursor nx = cur;
-    nx.next(a);
-    int64_t npg = 0;
-    int nvalid = 0;
-    if (!nx.done()) {
-      npg = nx.page(a);
-      nvalid = page_ok(a, npg) ? nx.valid() : 0;
-      D::load(raw_nxt, a, npg, nvalid, c, t);
-    }
-    const int buf = g % kTiles;
-    if (g >= kTiles && !sy.wait(B_TILE_EMPTY + buf, ((g / kTiles) - 1) & 1, false, 2)) return;
-    D::store(raw_cur, a, pg, valid, c, t, tiles + buf * kTileBytes);
+    Cursor nn = nx;
+    if (!nn.done()) nn.next(a);
+    const int64_t nnpg = nn.done() ? 0 : nn.page(a);
+    const int nvalid = nx.done() ? 0 : (page_ok(a, npg) ? nx.valid() : 0);
+    if (!nx.done()) D::load(raw_nxt, a, npg, nvalid, c, t);
+    const int kb = g % kKSlots, vb = g % kVSlots;
+    // the K slot was last used by page g - 2 (its Q.K^T completion is that barrier's previous
+    // phase), the V slot by page g - 3 (its P.V completion)
+    if (g >= kKSlots && !sy.wait(B_K_EMPTY + kb, ((g / kKSlots) - 1) & 1, false, 2)) return;
+    if (g >= kVSlots && !sy.wait(B_V_EMPTY + vb, ((g / kVSlots) - 1) & 1, false, 2)) return;
+    D::store(raw_cur, a, pg, valid, c, t, kring + kb * kKSlot, vring + vb * kVSlot);
     tc::fence_proxy_async_smem();
-    tc::mbar_arrive(sy.bar(B_TILE_FULL + buf));
+    // the V slot first: the Q.K^T threads wait only on the K slot and take it as "page written"
+    tc::mbar_arrive(sy.bar(B_V_FULL + vb));
+    tc::mbar_arrive(sy.bar(B_K_FULL + kb));
     raw_cur = raw_nxt;
     cur = nx;
+    nx = nn;
     pg = npg;
+    npg = nnpg;
     valid = nvalid;
   }
 }
 
-// MMA role (one thread). QK^T of page g and P.V of page g are issued in page order, each as soon as
-// its inputs are ready: QK(g) needs its operand tile, a free logit buffer (page g - 2 read out) and,
-// at a new request, the new Q; PV(g) needs P(g). Issuing whichever is ready keeps QK running ahead
-// while the softmax works, and cannot deadlock at segment boundaries.
-__device__ void role_mma(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, uint32_t tbase, uint32_t tiles,
-                         uint32_t pbuf, uint32_t qr) {
-  int total = 0;
-  for (int si = seg_b; si < seg_e; ++si) total += a.segs[si].num_pages;
-  Cursor cq, cp;
-  cq.begin(a, seg_b, seg_e);
-  cp.begin(a, seg_b, seg_e);
-  int gq = 0, gp = 0, qcount = 0, q_req = -1;
-  long long t_last = clock64();
-  while (gp < total) {
-    bool did = false;
-    if (gp < gq && mbar_test(sy.bar(B_P_FULL + (gp & 1)), (gp >> 1) & 1)) {
-      tc::tc_fence_after();
-      const int s = gp & 1, buf = gp % kTiles;
-      const uint32_t pa = pbuf + s * kPBytes, tv = tiles + buf * kTileBytes;
-      const bool first = cp.j == 0;
+// The 36 MMAs of one page's S = Q.K^T, issued back to back. The contraction runs over the latent
+// dims in this CTA's order: its own 256 nope dims (V slot atoms 0..3), the other 256 nope dims (K slot
+// atoms 0..3), then the rope dims (K slot atom 4); Q is stored in the same order (the first 384 of
+// them in TMEM, the rest in shared memory). Every operand is then a compile-time offset from a
+// per-page base, the same for both CTAs, so one unrolled body serves both.
+__device__ __forceinline__ void issue_qk(uint32_t ts, uint32_t tq, const tc::Desc2& kd, const tc::Desc2& vd,
+                                         const tc::Desc2& qd) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = tc::smem_desc(pa + 32 * kk, 16, 1024, tc::kSwizzle128);
-        const uint64_t bd = tc::smem_desc(tv + 2048 * kk, 8192, 1024, tc::kSwizzle128);
-        tc::mma_ss(tbase + TM_O, ad, bd, kIdescPV, (first && kk == 0) ? 0u : 1u);
-      }
-      tc::mma_commit(sy.bar(B_TILE_EMPTY + buf));
-      tc::mma_commit(sy.bar(B_P_FREE + s));
-      tc::mma_commit(sy.bar(B_O_DONE + s));
-      cp.next(a);
-      ++gp;
-      did = true;
-    } else if (gq < total) {
-      const bool newq = cq.j == 0 && cq.seg.req != q_req;
-      const int buf = gq % kTiles, s = gq & 1;
-      if (mbar_test(sy.bar(B_TILE_FULL + buf), (gq / kTiles) & 1) &&
-          (gq < 2 || mbar_test(sy.bar(B_S_FREE + s), ((gq >> 1) - 1) & 1)) &&
-          (!newq || mbar_test(sy.bar(B_Q_READY), qcount & 1))) {
-        tc::tc_fence_after();
-        const uint32_t td = tbase + TM_S + 64 * s, tk = tiles + buf * kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          const uint64_t bd = tc::smem_desc(tk + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, tc::kSwizzle128);
-          tc::mma_ts(td, tbase + TM_QN + 8 * ks, bd, kIdescQK, ks > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t ad = tc::smem_desc(qr + 32 * ks, 16, 512, tc::kSwizzle64);
-          const uint64_t bd = tc::smem_desc(tk + kRopeOff + 32 * ks, 16, 512, tc::kSwizzle64);
-          tc::mma_ss(td, ad, bd, kIdescQK, 1u);
-        }
-        tc::mma_commit(sy.bar(B_S_FULL + s));
-        if (newq) { q_req = cq.seg.req; ++qcount; }
-        cq.next(a);
-        ++gq;
-        did = true;
-      }
-    }
-    if (did) {
-      t_last = clock64();
-    } else if (((clock64() - t_last) & 0xFF) == 0 || clock64() - t_last > (1ll << 31)) {
-      if (*sy.abort) break;
-      if (clock64() - t_last > (1ll << 31)) {
-        *sy.abort = 1;
-        atomicOr(sy.status, 4);
-        break;
-      }
+  for (int ks = 0; ks < 36; ++ks) {             // permuted dims 16ks .. 16ks + 15
+    constexpr int kTm = kQTmemDims / 16;
+    const uint64_t b = ks < 16 ? vd.at((ks >> 2) * kAtom + 32 * (ks & 3))
+                               : kd.at(((ks - 16) >> 2) * kAtom + 32 * (ks & 3));
+    if (ks < kTm) {                             // A operand: Q from TMEM
+      if (ks == 0) tc::mma_ts_k<false>(ts, tq, b, kIdescQK);
+      else tc::mma_ts_k<true>(ts, tq + 8 * ks, b, kIdescQK);
+    } else {                                    // A operand: Q from shared memory
+      const int kq = ks - kTm;
+      tc::mma_ss_k<true>(ts, qd.at((kq >> 2) * kQAtom + 32 * (kq & 3)), b, kIdescQK);
     }
   }
-  // drain: every MMA issued so far has completed before TMEM is released
-  tc::mma_commit(sy.bar(B_FINAL));
-  sy.wait(B_FINAL, 0, false, 64);
 }
 
-// Softmax role, software-pipelined over pages: at page g it reads its partial logits S(g) from TMEM
-// and stores them straight into the peer's exchange buffer (stage 1), then finishes page g - 1
-// (stage 2): waits for the peer's partial of g - 1, adds the two in a fixed order, runs the online
-// softmax and writes P(g - 1). The remote stores of page g drain while stage 2 computes: the arrive
-// that frees the peer's buffer is relaxed (the values it guards have been used), and the
-// release-arrive that publishes page g comes last. Buffers are [16-byte chunk][head], so a warp's
-// remote store covers 512 contiguous bytes. Every wait is followed by a warp vote, so the warps stay
-// converged for the warp-collective tcgen05.ld / tcgen05.st and continue or give up as a whole.
-struct PendingPage {
-  int g, valid, j, last, partial, req;
-  float q_scale;
-};
+// MMA issue, split over two threads in different warps so that neither stream waits behind the
+// other: one thread issues S = Q.K^T page after page (each needs its operand tile, the logit buffer
+// read out for the previous page and, at a new request, the new Q), the other issues O += P.V as
+// soon as both halves of P have arrived. A tcgen05.commit tracks only the MMAs of the thread that
+// issues it, so each stream signals its own completions.
+__device__ void role_qk(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, int parity, uint32_t tbase,
+                        uint32_t kring, uint32_t vring, uint32_t qs, uint32_t qver) {
+  Cursor cq;
+  cq.begin(a, seg_b, seg_e);
+  const uint64_t k_desc0 = tc::smem_desc(kring, 16, 1024, tc::kSwizzle128);       // K-major, rows = tokens
+  const uint64_t v_desc0 = tc::smem_desc(vring, 16, 1024, tc::kSwizzle128);
+  const tc::Desc2 qd = tc::split_desc(tc::smem_desc(qs, 16, 1024, tc::kSwizzle128));   // K-major, rows = heads
+  // requests are counted over all pages (both parities), in the order the softmax loads their Q
+  int qcount = 0, q_req = -1, q_waited = -1;
+  for (int gq = 0; !cq.done(); ++gq, cq.next(a)) {
+    if (cq.j == 0 && cq.seg.req != q_req) { q_req = cq.seg.req; ++qcount; }
+    if ((gq & 1) != parity) continue;
+    const int kb = gq % kKSlots, vb = gq % kVSlots, s = gq & 1;
+    // K slot kb holds only pages of this parity, so this thread waits on each of its phases in turn;
+    // the dequant arrives on it after writing both rings of the page (the V slot included)
+    if (!sy.wait(B_K_FULL + kb, (gq / kKSlots) & 1, false, 4)) break;
+    // logit buffer s was last read out for page gq - 2 (also this thread's)
+    if (gq >= 2 && !sy.wait(B_S_FREE + s, ((gq >> 1) - 1) & 1, false, 4)) break;
+    // the Q rows of this page's request: the qcount-th request Q published by the softmax threads
+    if (q_waited != qcount) {
+      if (!wait_counter(sy, qver, static_cast<uint32_t>(qcount))) break;
+      q_waited = qcount;
+    }
+    tc::tc_fence_after();
+    const tc::Desc2 kd = tc::split_desc(tc::desc_add(k_desc0, kb * kKSlot));
+    const tc::Desc2 vd = tc::split_desc(tc::desc_add(v_desc0, vb * kVSlot));
+    issue_qk(tbase + TM_S + kHalf * s, tbase + TM_Q, kd, vd, qd);
+    tc::mma_commit(sy.bar(B_S_FULL + s));
+    tc::mma_commit(sy.bar(B_K_EMPTY + kb));
+  }
+  // drain: every MMA issued by this thread has completed before TMEM is released
+  tc::mma_commit(sy.bar(B_FINAL));
+}
 
+__device__ void role_pv(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, uint32_t tbase,
+                        uint32_t vring, uint32_t pbuf) {
+  Cursor cp;
+  cp.begin(a, seg_b, seg_e);
+  const uint64_t v_desc0 = tc::smem_desc(vring, kAtom, 1024, tc::kSwizzle128);    // MN-major (V), 4 dim atoms
+  const uint64_t p_desc0 = tc::smem_desc(pbuf, 16, 512, tc::kSwizzle64);          // K-major, rows = heads
+  for (int gp = 0; !cp.done(); ++gp) {
+    const int s = gp & 1, vb = gp % kVSlots;
+    if (!sy.wait(B_P_FULL + s, (gp >> 1) & 1, false, 4)) break;
+    // already complete (Q.K^T of this page waited for it); cannot advance before this P.V frees it
+    if (!sy.wait(B_V_FULL + vb, (gp / kVSlots) & 1, false, 4)) break;
+    tc::tc_fence_after();
+    const uint64_t pd = tc::desc_add(p_desc0, s * kPBytes);
+    const uint64_t vown = tc::desc_add(v_desc0, vb * kVSlot);
+    const uint64_t voth = tc::desc_add(v_desc0, vb * kVSlot + 4 * kAtom);
+    // tokens 16kk .. 16kk + 15: P half kk / 2, V rows from the own K tile or the other-token V tile
+    const uint64_t v0 = c == 0 ? vown : voth, v1 = c == 0 ? voth : vown;
+    if (cp.j == 0) tc::mma_ss_k<false>(tbase + TM_O, pd, v0, kIdescPV);
+    else tc::mma_ss_k<true>(tbase + TM_O, pd, v0, kIdescPV);
+    tc::mma_ss_k<true>(tbase + TM_O, tc::desc_add(pd, 32), tc::desc_add(v0, 2048), kIdescPV);
+    tc::mma_ss_k<true>(tbase + TM_O, tc::desc_add(pd, kPHalf), v1, kIdescPV);
+    tc::mma_ss_k<true>(tbase + TM_O, tc::desc_add(pd, kPHalf + 32), tc::desc_add(v1, 2048), kIdescPV);
+    tc::mma_commit(sy.bar(B_V_EMPTY + vb));
+    tc::mma_commit_multicast(sy.bar(B_P_FREE + s), 0x3);
+    tc::mma_commit(sy.bar(B_O_DONE + s));
+    cp.next(a);
+  }
+  tc::mma_commit(sy.bar(B_FINAL));
+}
+
+// Softmax role. Per page: logits of the own 32 tokens from TMEM, row maximum traded with the peer,
+// online softmax, own half of P written and copied to the peer. Every wait is followed by a warp
+// vote, so the warps stay converged for the warp-collective tcgen05.ld / tcgen05.st and continue or
+// give up as a whole.
+// The exchange buffers need no "free" barriers: the peer writes the row-maximum slot of page g + 2
+// (and the row-sum slot of a later segment end of the same parity) only after it has received this
+// CTA's row maxima of page g + 1, which this CTA sends after it has read the slot of page g.
 template <int KV>
 __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, int h,
-                             uint32_t tbase, uint32_t pbuf, uint32_t qr, uint32_t xbuf) {
+                             uint32_t tbase, uint32_t pbuf, uint32_t qs, uint32_t rm, uint32_t lx, uint32_t qver) {
   const uint32_t peer = c ^ 1u;
   const uint32_t tl = tbase + (static_cast<uint32_t>(h & ~31) << 16);   // this warp's TMEM lane quarter
   auto wait = [&](uint32_t bar, uint32_t parity, bool cluster, int code) -> bool {
     const bool ok = sy.wait(bar, parity, cluster, code);
     return __all_sync(0xffffffffu, ok);
   };
-  float m_used = -INFINITY, l = 0.0f;          // running softmax state of the segment in stage 2
-
-  // stage 2: finish page pp (own partial logits in `own`, the peer's in the local exchange buffer)
-  auto finish = [&](const PendingPage& pp, const uint32_t (&own)[64]) -> bool {
-    const int b = pp.g, s = b & 1;
-    if (pp.j == 0) { m_used = -INFINITY; l = 0.0f; }
-    if (!wait(B_X_FULL + s, (b >> 1) & 1, true, 256)) return false;
-    const uint32_t xb = xbuf + s * kXBytes + h * 16;
-    float x[64];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint4 pv = lds128(xb + i * 2048);
-      const uint32_t p4[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float mine = __uint_as_float(own[4 * i + u]), theirs = __uint_as_float(p4[u]);
-        x[4 * i + u] = c == 0 ? (mine + theirs) : (theirs + mine);
-      }
-    }
-    tc::mbar_arrive_cluster_relaxed(sy.bar(B_X_FREE + s), peer);   // the peer may refill this buffer
-    // row maximum of the raw logit sums (the scale is positive), as a tree for ILP
-    float mx8[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      if (i >= pp.valid) x[i] = -INFINITY;
-      mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
-    }
-#pragma unroll
-    for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int u = 0; u < w; ++u) mx8[u] = fmaxf(mx8[u], mx8[u + w]);
-    const float rmax = mx8[0] * pp.q_scale;
-    const bool renew = rmax > -INFINITY && (m_used == -INFINITY || rmax > m_used + 8.0f);
-    const float alpha = renew ? dev::fast_exp2(m_used - rmax) : 1.0f;   // 0 when m_used is -inf
-    // O holds earlier pages of this segment scaled to the old maximum: rescale the rows that renew
-    // (the whole warp takes part in the TMEM traffic) once PV(b - 1) has completed
-    const bool rescale_row = renew && pp.j > 0 && m_used != -INFINITY;
-    if (__any_sync(0xffffffffu, rescale_row)) {
-      if (!wait(B_O_DONE + ((b - 1) & 1), ((b - 1) >> 1) & 1, false, 512)) return false;
-      tc::tc_fence_after();
-      const float f = rescale_row ? alpha : 1.0f;
-#pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t orow[32];
-        tc::tmem_ld32(tl + TM_O + 32 * cc, orow);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int u = 0; u < 32; ++u) orow[u] = __float_as_uint(__uint_as_float(orow[u]) * f);
-        tc::tmem_st32(tl + TM_O + 32 * cc, orow);
-      }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-    }
-    if (renew) {
-      l *= alpha;
-      m_used = rmax;
-    }
-    const float mref = m_used == -INFINITY ? 0.0f : m_used;
-    uint32_t pk[32];
-    float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {   // p = 2^(x * scale - m): one FMA and one exp2 per logit
-      const float p0 = dev::fast_exp2(fmaf(x[2 * i], pp.q_scale, -mref));
-      const float p1 = dev::fast_exp2(fmaf(x[2 * i + 1], pp.q_scale, -mref));
-      l4[i & 3] += p0 + p1;
-      pk[i] = dev::pack_f16x2(p0, p1);
-    }
-    l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-    if (b >= 2 && !wait(B_P_FREE + s, ((b >> 1) - 1) & 1, false, 1024)) return false;
-    const uint32_t prow = pbuf + s * kPBytes;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) sts128(prow + tc::sw128_offset(h, i), make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]));
-    tc::fence_proxy_async_smem();
-    tc::mbar_arrive(sy.bar(B_P_FULL + s));
-    if (!pp.last) return true;
-    // ---- segment epilogue: O / l for this CTA's 256 output dims ----
-    if (!wait(B_O_DONE + s, (b >> 1) & 1, false, 2048)) return false;
-    tc::tc_fence_after();
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    const float lse2 = l > 0.0f ? m_used + __log2f(l) : -INFINITY;
-    const int64_t row = static_cast<int64_t>(pp.req) * a.heads + h;
-#pragma unroll 1
-    for (int cc = 0; cc < 8; ++cc) {
-      uint32_t orow[32];
-      tc::tmem_ld32(tl + TM_O + 32 * cc, orow);
-      tc::tmem_wait_ld();
-      if (pp.partial < 0) {
-        const float sc = inv * a.out_scale;
-        uint4* dst = reinterpret_cast<uint4*>(a.out + row * kDv + 256 * c + 32 * cc);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          dst[u] = make_uint4(dev::pack_bf16x2(__uint_as_float(orow[8 * u]) * sc, __uint_as_float(orow[8 * u + 1]) * sc),
-                              dev::pack_bf16x2(__uint_as_float(orow[8 * u + 2]) * sc, __uint_as_float(orow[8 * u + 3]) * sc),
-                              dev::pack_bf16x2(__uint_as_float(orow[8 * u + 4]) * sc, __uint_as_float(orow[8 * u + 5]) * sc),
-                              dev::pack_bf16x2(__uint_as_float(orow[8 * u + 6]) * sc, __uint_as_float(orow[8 * u + 7]) * sc));
-      } else {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(pp.partial) * a.heads + h) * kDv + 256 * c + 32 * cc);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          dst[u] = make_float4(__uint_as_float(orow[4 * u]) * inv, __uint_as_float(orow[4 * u + 1]) * inv,
-                               __uint_as_float(orow[4 * u + 2]) * inv, __uint_as_float(orow[4 * u + 3]) * inv);
-      }
-    }
-    tc::tc_fence_before();
-    if (c == 0) {
-      if (pp.partial < 0) { if (a.lse) a.lse[row] = lse2 * 0.69314718055994531f; }
-      else a.part_lse[static_cast<int64_t>(pp.partial) * a.heads + h] = lse2;
-    }
-    return true;
-  };
-
+  float m_used = -INFINITY, l = 0.0f;          // running softmax state of the segment
+  int lx_count[2] = {0, 0};                    // segment ends seen at even / odd pages
   Cursor cur;
   cur.begin(a, seg_b, seg_e);
-  int cur_req = -1;
+  int cur_req = -1, nq = 0;
   float q_scale = a.scale_log2;
-  PendingPage pend{};
-  bool have = false;
-  uint32_t own_prev[64];
+  int64_t pg = cur.done() ? 0 : cur.page(a);
   for (int g = 0; !cur.done(); ++g) {
     const Segment seg = cur.seg;
     if (cur.j == 0 && seg.req != cur_req) {
@@ -512,65 +503,189 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       if (mx != 0u && mx < 0x7F80u) sh = max(-100, min(113, static_cast<int>(mx >> 7) - 127 - 14));
       const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
       q_scale = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
-#pragma unroll
-      for (int part = 0; part < 4; ++part) {          // 4 x 64 nope dims -> 4 x 32 TMEM columns
+      // latent dim of position d in this CTA's contraction order (own nope dims, other nope dims, rope)
+      auto perm = [c](int d) { return d < 256 ? 256 * c + d : (d < 512 ? 256 * (1 - c) + d - 256 : d); };
+#pragma unroll 1
+      for (int part = 0; part < kQTmemDims / 64; ++part) {   // 64 dims -> 32 TMEM columns
         uint32_t r[32];
+        const uint8_t* src = qrow + perm(64 * part) * 2;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qrow + (256 * c + 64 * part + 8 * i) * 2);
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * i);
           r[4 * i] = dev::bf16x2_to_f16x2(v.x, down);
           r[4 * i + 1] = dev::bf16x2_to_f16x2(v.y, down);
           r[4 * i + 2] = dev::bf16x2_to_f16x2(v.z, down);
           r[4 * i + 3] = dev::bf16x2_to_f16x2(v.w, down);
         }
         __syncwarp();
-        tc::tmem_st32(tl + TM_QN + 32 * part, r);
+        tc::tmem_st32(tl + TM_Q + 32 * part, r);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {                   // 32 rope dims -> one 64-byte row
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + (512 + 32 * c + 8 * i) * 2);
-        sts128(qr + tc::sw64_offset(h, i), make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
-                                                     dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
+      for (int i = 0; i < 8 * kQSmemAtoms; ++i) {     // positions 384..575 -> 64-dim atoms, row h
+        const uint4 v = *reinterpret_cast<const uint4*>(qrow + (perm(kQTmemDims + 64 * (i >> 3)) + 8 * (i & 7)) * 2);
+        sts128(qs + (i >> 3) * kQAtom + tc::sw128_offset(h, i & 7),
+               make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
+                          dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
       }
       tc::tmem_wait_st();
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       tc::mbar_arrive(sy.bar(B_Q_READY));
+      // thread 0 sees every phase of Q_READY in turn (all 128 rows written) and publishes the count
+      bool ok = true;
+      if (h == 0) {
+        ok = sy.wait(B_Q_READY, nq & 1, false, 16);
+        if (ok) tc::st_release_u32(qver, static_cast<uint32_t>(nq + 1));
+      }
+      if (!__all_sync(0xffffffffu, ok)) return;
+      ++nq;
       cur_req = seg.req;
     }
-    const int64_t pg = cur.page(a);
-    PendingPage now;
-    now.g = g;
-    now.valid = page_ok(a, pg) ? cur.valid() : 0;
-    now.j = cur.j;
-    now.last = cur.j == seg.num_pages - 1;
-    now.partial = seg.partial;
-    now.req = seg.req;
-    now.q_scale = q_scale;
-    // ---- stage 1: this page's partial logits into the local exchange buffer ----
+    if (cur.j == 0) { m_used = -INFINITY; l = 0.0f; }
+    const int valid = page_ok(a, pg) ? cur.valid() : 0;
+    Cursor nx = cur;                 // the next page's table entries load while this page runs
+    nx.next(a);
+    const int64_t npg = nx.done() ? 0 : nx.page(a);
+    const int nv = min(max(valid - kHalf * c, 0), kHalf);
+    const bool last = cur.j == seg.num_pages - 1;
     const int s = g & 1;
+
+    // ---- logits of the own tokens (buffer s; refilled for page g + 2 only after S_FREE(s)) ----
     if (!wait(B_S_FULL + s, (g >> 1) & 1, false, 128)) return;
     tc::tc_fence_after();
-    uint32_t sr[64];
-    tc::tmem_ld32(tl + TM_S + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-    tc::tmem_ld32(tl + TM_S + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+    uint32_t sr[32];
+    tc::tmem_ld32(tl + TM_S + kHalf * s, sr);
     tc::tmem_wait_ld();
     tc::tc_fence_before();
     tc::mbar_arrive(sy.bar(B_S_FREE + s));
-    if (g >= 2 && !wait(B_X_FREE + s, ((g >> 1) - 1) & 1, true, 4096)) return;
-    const uint32_t xremote = tc::mapa(xbuf + s * kXBytes + h * 16, peer);
+    float x[32], mx8[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) tc::st_cluster_v4(xremote + i * 2048, sr[4 * i], sr[4 * i + 1], sr[4 * i + 2], sr[4 * i + 3]);
-    // ---- stage 2: the previous page, while the remote stores drain ----
-    if (have && !finish(pend, own_prev)) return;
-    tc::mbar_arrive_cluster(sy.bar(B_X_FULL + s), peer);   // release: publishes this page's logits
+    for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) own_prev[i] = sr[i];
-    pend = now;
-    have = true;
-    cur.next(a);
+    for (int i = 0; i < 32; ++i) {
+      x[i] = i < nv ? __uint_as_float(sr[i]) : -INFINITY;
+      mx8[i & 7] = fmaxf(mx8[i & 7], x[i]);
+    }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int u = 0; u < w; ++u) mx8[u] = fmaxf(mx8[u], mx8[u + w]);
+    const float r_own = mx8[0];
+
+    // ---- trade row maxima: both CTAs take the same maximum and make the same rescale decision ----
+    tc::st_async_f32(rm + s * 512 + 4 * h, r_own, sy.bar(B_RM_FULL + s), peer);
+    if (h == 0) tc::mbar_arrive_expect_tx(sy.bar(B_RM_FULL + s), 512);
+    // p = 2^(x * scale - m): one FMA and one exp2 per logit. While the peer's maximum is in flight,
+    // compute P against the current running maximum; when the agreed maximum keeps it (no rescale,
+    // almost every page after a segment's first), these are exactly the values computed after the wait.
+    uint32_t pk[16];
+    float lsum = 0.0f;
+    auto exp_row = [&](float mref) {
+      float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float p0 = dev::fast_exp2(fmaf(x[2 * i], q_scale, -mref));
+        const float p1 = dev::fast_exp2(fmaf(x[2 * i + 1], q_scale, -mref));
+        l4[i & 3] += p0 + p1;
+        pk[i] = dev::pack_f16x2(p0, p1);
+      }
+      lsum = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+    };
+    const bool spec = m_used != -INFINITY && !(r_own * q_scale > m_used + 8.0f);
+    if (spec) exp_row(m_used);
+    if (!wait(B_RM_FULL + s, (g >> 1) & 1, true, 256)) return;
+    const float r_peer = tc::lds_f32(rm + s * 512 + 4 * h);
+    const float rmax = fmaxf(r_own, r_peer) * q_scale;
+    const bool renew = rmax > -INFINITY && (m_used == -INFINITY || rmax > m_used + 8.0f);
+    const float alpha = renew ? dev::fast_exp2(m_used - rmax) : 1.0f;   // 0 when m_used is -inf
+    // O holds earlier pages of this segment scaled to the old maximum: rescale the rows that renew
+    // (the whole warp takes part in the TMEM traffic) once PV(g - 1) has completed
+    const bool rescale_row = renew && cur.j > 0 && m_used != -INFINITY;
+    if (__any_sync(0xffffffffu, rescale_row)) {
+      if (!wait(B_O_DONE + ((g - 1) & 1), ((g - 1) >> 1) & 1, false, 512)) return;
+      tc::tc_fence_after();
+      const float f = rescale_row ? alpha : 1.0f;
+#pragma unroll 1
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t orow[32];
+        tc::tmem_ld32(tl + TM_O + 32 * cc, orow);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) orow[u] = __float_as_uint(__uint_as_float(orow[u]) * f);
+        tc::tmem_st32(tl + TM_O + 32 * cc, orow);
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+    }
+    if (renew) {
+      l *= alpha;
+      m_used = rmax;
+    }
+    if (!spec || renew) exp_row(m_used == -INFINITY ? 0.0f : m_used);
+    l += lsum;
+
+    // ---- own half of P: local buffer, then one bulk copy into the peer's buffer. P_FREE(s) counts
+    // the P.V of page g - 2 in both CTAs (both read this buffer pair) ----
+    if (g >= 2 && !wait(B_P_FREE + s, ((g >> 1) - 1) & 1, false, 1024)) return;
+    const uint32_t prow = pbuf + s * kPBytes + c * kPHalf;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) sts128(prow + tc::sw64_offset(h, u), make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive(sy.bar(B_P_LOCAL + s));
+    bool ok = true;
+    if (h == 0) {
+      ok = sy.wait(B_P_LOCAL + s, (g >> 1) & 1, false, 8192);
+      if (ok) {
+        tc::bulk_copy_to_peer(prow, prow, kPHalf, sy.bar(B_P_FULL + s), peer);
+        tc::mbar_arrive_expect_tx(sy.bar(B_P_FULL + s), kPHalf);   // completes with the peer's half
+      }
+    }
+    if (!__all_sync(0xffffffffu, ok)) return;
+    cur = nx;
+    pg = npg;
+    if (!last) continue;
+
+    // ---- segment end: trade row sums (fixed order of the two terms), then O / l for this CTA's
+    // 256 output dims once PV(g) has completed ----
+    tc::st_async_f32(lx + s * 512 + 4 * h, l, sy.bar(B_LX_FULL + s), peer);
+    if (h == 0) tc::mbar_arrive_expect_tx(sy.bar(B_LX_FULL + s), 512);
+    if (!wait(B_LX_FULL + s, lx_count[s] & 1, true, 4096)) return;
+    ++lx_count[s];
+    const float l_peer = tc::lds_f32(lx + s * 512 + 4 * h);
+    const float lt = c == 0 ? l + l_peer : l_peer + l;
+    if (!wait(B_O_DONE + s, (g >> 1) & 1, false, 2048)) return;
+    tc::tc_fence_after();
+    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+    const float lse2 = lt > 0.0f ? m_used + __log2f(lt) : -INFINITY;
+    const int64_t row = static_cast<int64_t>(seg.req) * a.heads + h;
+#pragma unroll 1
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t orow[32];
+      tc::tmem_ld32(tl + TM_O + 32 * cc, orow);
+      tc::tmem_wait_ld();
+      if (seg.partial < 0) {
+        const float sc = inv * a.out_scale;
+        uint4* dst = reinterpret_cast<uint4*>(a.out + row * kDv + 256 * c + 32 * cc);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          dst[u] = make_uint4(dev::pack_bf16x2(__uint_as_float(orow[8 * u]) * sc, __uint_as_float(orow[8 * u + 1]) * sc),
+                              dev::pack_bf16x2(__uint_as_float(orow[8 * u + 2]) * sc, __uint_as_float(orow[8 * u + 3]) * sc),
+                              dev::pack_bf16x2(__uint_as_float(orow[8 * u + 4]) * sc, __uint_as_float(orow[8 * u + 5]) * sc),
+                              dev::pack_bf16x2(__uint_as_float(orow[8 * u + 6]) * sc, __uint_as_float(orow[8 * u + 7]) * sc));
+      } else {
+        float4* dst = reinterpret_cast<float4*>(a.part_o + (static_cast<int64_t>(seg.partial) * a.heads + h) * kDv + 256 * c + 32 * cc);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          dst[u] = make_float4(__uint_as_float(orow[4 * u]) * inv, __uint_as_float(orow[4 * u + 1]) * inv,
+                               __uint_as_float(orow[4 * u + 2]) * inv, __uint_as_float(orow[4 * u + 3]) * inv);
+      }
+    }
+    tc::tc_fence_before();
+    if (c == 0) {
+      if (seg.partial < 0) { if (a.lse) a.lse[row] = lse2 * 0.69314718055994531f; }
+      else a.part_lse[static_cast<int64_t>(seg.partial) * a.heads + h] = lse2;
+    }
   }
-  if (have) finish(pend, own_prev);
 }
 
 template <int KV>
@@ -589,24 +704,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
   sy.status = a.status;
 
   if (tid == 0) {
-    for (int i = 0; i < 3; ++i) { tc::mbar_init(sy.bar(B_TILE_FULL + i), kDQ); tc::mbar_init(sy.bar(B_TILE_EMPTY + i), 1); }
+    for (int i = 0; i < kKSlots; ++i) { tc::mbar_init(sy.bar(B_K_FULL + i), kDQ); tc::mbar_init(sy.bar(B_K_EMPTY + i), 1); }
+    for (int i = 0; i < kVSlots; ++i) { tc::mbar_init(sy.bar(B_V_FULL + i), kDQ); tc::mbar_init(sy.bar(B_V_EMPTY + i), 1); }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(sy.bar(B_S_FULL + i), 1);
       tc::mbar_init(sy.bar(B_S_FREE + i), 128);
-      tc::mbar_init(sy.bar(B_P_FULL + i), 128);
-      tc::mbar_init(sy.bar(B_P_FREE + i), 1);
-      tc::mbar_init(sy.bar(B_X_FULL + i), 128);
+      tc::mbar_init(sy.bar(B_P_LOCAL + i), 128);
+      tc::mbar_init(sy.bar(B_P_FULL + i), 1);        // plus the peer's 8 KB of P, counted in bytes
+      tc::mbar_init(sy.bar(B_P_FREE + i), 2);        // P.V of the page in both CTAs
+      tc::mbar_init(sy.bar(B_O_DONE + i), 1);
+      tc::mbar_init(sy.bar(B_RM_FULL + i), 1);       // plus the peer's 128 x 4 bytes, counted in bytes
+      tc::mbar_init(sy.bar(B_LX_FULL + i), 1);
     }
-    tc::mbar_init(sy.bar(B_O_DONE), 1);
-    tc::mbar_init(sy.bar(B_O_DONE + 1), 1);
     tc::mbar_init(sy.bar(B_Q_READY), 128);
-    tc::mbar_init(sy.bar(B_X_FREE), 128);
-    tc::mbar_init(sy.bar(B_X_FREE + 1), 128);
-    tc::mbar_init(sy.bar(B_FINAL), 1);
+    tc::mbar_init(sy.bar(B_FINAL), 3);             // one commit per MMA-issuing thread
     *sy.abort = 0;
+    *reinterpret_cast<volatile uint32_t*>(sbase + OFF_QVER) = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 7) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(base + OFF_TSLOT, 512);
     tc::tmem_relinquish();
   }
@@ -617,18 +733,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(sbase + OFF_TSLOT);
 
   if (warp < 4) {
-    role_softmax<KV>(a, sy, seg_b, seg_e, c, tid, tbase, base + OFF_P, base + OFF_QR, base + OFF_X);
-  } else if (warp < 7) {
-    role_dequant<KV>(a, sy, seg_b, seg_e, c, tid - 128, base + OFF_TILE);
+    role_softmax<KV>(a, sy, seg_b, seg_e, c, tid, tbase, base + OFF_P, base + OFF_Q, base + OFF_RM, base + OFF_LX,
+                     base + OFF_QVER);
+  } else if (warp < kQkWarpOdd) {
+    role_dequant<KV>(a, sy, seg_b, seg_e, c, tid - 128, base + OFF_K, base + OFF_V);
+  } else if (warp == kPvWarp) {
+    if ((tid & 31) == 0) role_pv(a, sy, seg_b, seg_e, c, tbase, base + OFF_V, base + OFF_P);
   } else if ((tid & 31) == 0) {
-    role_mma(a, sy, seg_b, seg_e, tbase, base + OFF_TILE, base + OFF_P, base + OFF_QR);
+    role_qk(a, sy, seg_b, seg_e, c, warp == kQkWarpOdd ? 1 : 0, tbase, base + OFF_K, base + OFF_V, base + OFF_Q,
+            base + OFF_QVER);
   }
+  // every MMA of the three issuing threads has completed before TMEM is released
+  if (warp >= kQkWarpOdd && (tid & 31) == 0) sy.wait(B_FINAL, 0, false, 64);
   __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 7) {
+  if (warp == kMmaWarp) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tbase, 512);
+  }
+  // After a timeout a bulk copy into the peer may still be in flight: give it time to land before
+  // either CTA of the pair releases its shared memory. Normal runs consume every copy they issue.
+  if (tid == 0) {
+    const int peer_abort = tc::ld_cluster_u32(tc::mapa(base + OFF_ABORT, static_cast<uint32_t>(c ^ 1)));
+    if (*sy.abort || peer_abort) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 200000) {}
+    }
   }
   tc::cluster_sync();          // no CTA leaves while its peer may still touch its shared memory
 }

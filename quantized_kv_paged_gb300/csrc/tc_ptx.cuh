@@ -85,6 +85,61 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
+}
+
+// Asynchronous 4-byte store into CTA `rank` of the cluster at the offset `dst_local`, counted as 4
+// transaction bytes on that CTA's mbarrier at offset `bar_local` (no fence: the receiver learns of
+// the value only through the barrier).
+__device__ __forceinline__ void st_async_f32(uint32_t dst_local, float v, uint32_t bar_local, uint32_t rank) {
+  asm volatile("{\n\t.reg .b32 rd, rb;\n\t"
+               "mapa.shared::cluster.u32 rd, %0, %3;\n\t"
+               "mapa.shared::cluster.u32 rb, %2, %3;\n\t"
+               "st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [rd], %1, [rb];\n\t}"
+               :: "r"(dst_local), "f"(v), "r"(bar_local), "r"(rank) : "memory");
+}
+
+__device__ __forceinline__ int ld_cluster_u32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Arrive on a local mbarrier and raise its expected transaction count by `bytes` (the bytes that
+// asynchronous copies will deliver before the phase can complete).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(bar), "r"(bytes) : "memory");
+}
+
+// Asynchronous bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory to the same offset in CTA `rank` of the cluster; completion is counted in
+// bytes on the mbarrier at offset `bar_local` of that CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_local, uint32_t src_local, uint32_t bytes,
+                                                  uint32_t bar_local, uint32_t rank) {
+  asm volatile("{\n\t.reg .b32 rd, rb;\n\t"
+               "mapa.shared::cluster.u32 rd, %0, %3;\n\t"
+               "mapa.shared::cluster.u32 rb, %2, %3;\n\t"
+               "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [rd], [%1], %4, [rb];\n\t}"
+               :: "r"(dst_local), "r"(src_local), "r"(bar_local), "r"(rank), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
@@ -184,9 +239,47 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
                :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// The same two forms with the accumulate flag fixed at compile time (nothing but the MMA is issued).
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ss_k(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  if (kAccumulate)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc) : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc) : "memory");
+}
+template <bool kAccumulate>
+__device__ __forceinline__ void mma_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+  if (kAccumulate)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc) : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc) : "memory");
+}
+
+// A shared-memory descriptor advanced by `bytes` (start address field only; stays inside the
+// 14-bit field for any address below 256 KB).
+__host__ __device__ constexpr uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
+// The same on a descriptor held as two 32-bit halves: the start address lives in the low half, and
+// adding there cannot carry out of it (see above), so one 32-bit add per operand suffices.
+struct Desc2 {
+  uint32_t lo, hi;
+  __device__ __forceinline__ uint64_t at(uint32_t bytes) const {
+    return (static_cast<uint64_t>(hi) << 32) | static_cast<uint64_t>(lo + (bytes >> 4));
+  }
+};
+__device__ __forceinline__ Desc2 split_desc(uint64_t d) {
+  return Desc2{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
 // Arrive once on the mbarrier when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+// The same, arriving on the mbarrier at this offset in every CTA of the cluster named in `cta_mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               :: "r"(bar), "h"(cta_mask) : "memory");
 }
 
 // ---- swizzled shared-memory layouts ---------------------------------------------------------------

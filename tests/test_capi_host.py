@@ -115,5 +115,16 @@ def test_run_and_append_reject_before_launch(lib):
     assert f(17, 1, 4, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID      # misaligned source
     assert f(16, 1, -1, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID
     assert f(16, 1, 0, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_OK              # nothing to do
+    # a plan with a valid header but an output that is only 4-byte aligned: refused before launch
+    # (the attend kernels store 16-byte vectors)
+    pv = plan(np.array([0, 2], np.int32), np.array([100], np.int32))
+    pv.magic = 0x716B76702D706C31
+    st = lib.mla_decode_attend(ctypes.byref(pv), 16, 16, None, 10, 16, 0.1, 1.0, 0x1004, None, 256,
+                               pv.workspace_bytes, None)
+    assert st == q.QKVP_E_INVALID
+    # a pool that is 16- but not 32-byte aligned (the attend kernels use 32-byte loads)
+    st = lib.mla_decode_attend(ctypes.byref(pv), 16, 0x1010, None, 10, 16, 0.1, 1.0, 0x1000, None, 256,
+                               pv.workspace_bytes, None)
+    assert st == q.QKVP_E_INVALID
     assert lib.kv_pool_cast_bf16(16, 17, 16, None) == q.QKVP_E_INVALID
     assert lib.qkvp_encode_f32(16, 4, 3, 16, None) == q.QKVP_E_INVALID
