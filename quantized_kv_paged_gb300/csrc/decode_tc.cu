@@ -593,6 +593,16 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
     };
     const bool spec = m_used != -INFINITY && !(r_own * q_scale > m_used + 8.0f);
     if (spec) exp_row(m_used);
+    // own half of P goes to the local buffer s, then one bulk copy into the peer's buffer. P_FREE(s)
+    // counts the P.V of page g - 2 in both CTAs (both read this buffer pair). The speculative row is
+    // stored while the peer's maximum is still in flight and rewritten below if it does not hold.
+    if (g >= 2 && !wait(B_P_FREE + s, ((g >> 1) - 1) & 1, false, 1024)) return;
+    const uint32_t prow = pbuf + s * kPBytes + c * kPHalf;
+    auto store_row = [&]() {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sts128(prow + tc::sw64_offset(h, u), make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
+    };
+    if (spec) store_row();
     if (!wait(B_RM_FULL + s, (g >> 1) & 1, true, 256)) return;
     const float r_peer = tc::lds_f32(rm + s * 512 + 4 * h);
     const float rmax = fmaxf(r_own, r_peer) * q_scale;
@@ -621,15 +631,11 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       l *= alpha;
       m_used = rmax;
     }
-    if (!spec || renew) exp_row(m_used == -INFINITY ? 0.0f : m_used);
+    if (!spec || renew) {
+      exp_row(m_used == -INFINITY ? 0.0f : m_used);
+      store_row();
+    }
     l += lsum;
-
-    // ---- own half of P: local buffer, then one bulk copy into the peer's buffer. P_FREE(s) counts
-    // the P.V of page g - 2 in both CTAs (both read this buffer pair) ----
-    if (g >= 2 && !wait(B_P_FREE + s, ((g >> 1) - 1) & 1, false, 1024)) return;
-    const uint32_t prow = pbuf + s * kPBytes + c * kPHalf;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) sts128(prow + tc::sw64_offset(h, u), make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]));
     tc::fence_proxy_async_smem();
     tc::mbar_arrive(sy.bar(B_P_LOCAL + s));
     bool ok = true;
