@@ -22,6 +22,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -207,6 +208,60 @@ class Problem:
         q.mla_decode_combine(self.plan, self.g, self.out, self.lse, self.ws)
 
 
+def with_heads(w, heads: int):
+    """The same pool and page table with only the first `heads` query heads."""
+    return dataclasses.replace(w, q=w.q[:, :heads, :].contiguous(), heads=heads)
+
+
+def heads_sweep(q, pk, w, kv, args, steps, g=1.0, min_splits=0, heads=(16, 32, 64)):
+    """Decode of one workload shape at fewer query heads. Below 128 heads the mma.sync kernel runs
+    (the tcgen05 kernel needs 128), and the KV bytes stay the same while the flops shrink, so the
+    step moves from the tensor-bound to the HBM-bound side of the roofline."""
+    out = {}
+    for h in heads:
+        pb = Problem(q, with_heads(w, h), kv, g=g, min_splits=min_splits, algo=args.algo)
+        ms, att = time_problem(pb, steps, args.warmup)
+        r = summarize(pb, ms, att, pk)
+        t_hbm = pb.kv_bytes / (pk["hbm_gbs"] * 1e9) * 1e6
+        t_tc = pb.flops / (pk["bf16_tflops"] * 1e12) * 1e6
+        r["binding"] = "hbm" if t_hbm >= t_tc else "tensor"
+        r["floor_us"] = round(max(t_hbm, t_tc), 2)
+        r["frac_of_binding_floor"] = round(max(t_hbm, t_tc) / r["decode_kernel_us"], 4)
+        r["algo"] = "tcgen05" if pb.plan.algo == 2 else "mma_sync"
+        out[f"h{h}"] = r
+        del pb
+    torch.cuda.empty_cache()
+    return out
+
+
+def extend_gather(q, pk, w, kv, data, scale, g, steps, warmup):
+    """The extend path's gather: every request's whole cached prefix into one FP8 E4M3 workspace
+    (kv_gather_fp8). Bytes moved per call = pool bytes read (576 or 324 per token) + 576 written."""
+    dev = w.pool_fp8.device
+    tok = np.concatenate([[0], np.cumsum(w.kv_len)]).astype(np.int64)
+    ip = torch.from_numpy(w.kv_indptr.astype(np.int32)).to(dev)
+    ix = torch.from_numpy(w.kv_indices).to(dev)
+    tk = torch.from_numpy(tok).to(dev)
+    out = torch.empty((int(tok[-1]), LATENT), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        q.kv_gather_fp8(data, scale, kv, g, ip, ix, tk, out, num_pages=w.num_pages)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        q.kv_gather_fp8(data, scale, kv, g, ip, ix, tk, out, num_pages=w.num_pages)
+        b.record()
+    torch.cuda.synchronize()
+    ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+    tokens = int(tok[-1])
+    moved = tokens * ((LATENT if kv == q.KV_FP8_E4M3 else 324) + LATENT)
+    del out
+    torch.cuda.empty_cache()
+    return {"us": round(ms * 1e3, 2), "tokens": tokens, "workspace_bytes": tokens * LATENT, "bytes_moved": moved,
+            "gbs": round(moved / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac_of_measured": round(moved / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+
+
 def time_problem(pb: Problem, steps: int, warmup: int, world: int = 1):
     for _ in range(warmup):
         pb.step()
@@ -390,7 +445,7 @@ def main():
     gpu_launches = args.steps * pb.launches_per_step()
     extra = {}
     if rank == 0 and world == 1 and not args.no_extra:
-        extra = extra_workloads(q, pk, dev, args, host_main=None)
+        extra = extra_workloads(q, pk, dev, args, main_w=w)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = oracle_sample(w, (w.pool_fp8.cpu().numpy(), None))
@@ -418,15 +473,23 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def extra_workloads(q, pk, dev, args, host_main=None):
+def extra_workloads(q, pk, dev, args, main_w=None):
     steps = max(10, min(args.steps, 50))
     res = {}
+    # heads sweep of the headline shape (FP8 44 x 32K) at 16 / 32 / 64 heads
+    if main_w is not None:
+        res["heads_sweep_mla_fp8_b44_l32k"] = heads_sweep(q, pk, main_w, q.KV_FP8_E4M3, args, steps)
     # NVFP4, 10 x 163,840 (+1 appended per step), 128 heads
     w = synth.workload("mla_nvfp4_b10_h128_l160k", device=dev)
     pb = Problem(q, w, q.KV_NVFP4, g=1.0, append=True, algo=args.algo)
     ms, att = time_problem(pb, steps, args.warmup)
     res["mla_nvfp4_b10_h128_l160k"] = summarize(pb, ms, att, pk)
-    del pb, w
+    del pb
+    res["heads_sweep_mla_nvfp4_b10_l160k"] = heads_sweep(q, pk, w, q.KV_NVFP4, args, steps)
+    nv = Problem(q, w, q.KV_NVFP4, g=1.0)
+    res["extend_gather_nvfp4_b10_l160k"] = extend_gather(q, pk, w, q.KV_NVFP4, nv.data, nv.scale, 1.0, steps, args.warmup)
+    res["extend_gather_fp8_b10_l160k"] = extend_gather(q, pk, w, q.KV_FP8_E4M3, w.pool_fp8, None, 1.0, steps, args.warmup)
+    del nv, w
     torch.cuda.empty_cache()
     # NVFP4, 1 x 1,048,576, >= 148 splits, global scale 1 and calibrated
     w = synth.workload("mla_nvfp4_b1_h128_l1m", device=dev)
@@ -437,6 +500,7 @@ def extra_workloads(q, pk, dev, args, host_main=None):
         r["global_scale"] = g
         res[f"mla_nvfp4_b1_h128_l1m_{tag}"] = r
         del pb
+    res["heads_sweep_mla_nvfp4_b1_l1m"] = heads_sweep(q, pk, w, q.KV_NVFP4, args, steps, min_splits=148)
     del w
     torch.cuda.empty_cache()
     # mixed serving batch: fused FP8 decode vs cast-then-attend (pool cast to BF16 + BF16 decode)
@@ -444,31 +508,75 @@ def extra_workloads(q, pk, dev, args, host_main=None):
     fused = Problem(q, w, q.KV_FP8_E4M3, algo=args.algo)
     ms, att = time_problem(fused, steps, args.warmup)
     r = summarize(fused, ms, att, pk)
-    base = Problem(q, w, q.KV_BF16, algo=args.algo)
-    cast_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for _ in range(args.warmup):
-        q.kv_pool_cast_bf16(w.pool_fp8, base.data)
-        base.step()
-    torch.cuda.synchronize()
-    for k in range(steps):
-        cast_ev[k][0].record()
-        q.kv_pool_cast_bf16(w.pool_fp8, base.data)
-        cast_ev[k][1].record()
-        dec_ev[k][0].record()
-        base.step()
-        dec_ev[k][1].record()
-    torch.cuda.synchronize()
-    cast_ms = float(np.mean([a.elapsed_time(b) for a, b in cast_ev]))
-    bdec_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
+    # the baseline's BF16 decode runs with whichever kernel family is faster on it
+    best = None
+    for algo in (q.ALGO_MMA_SYNC, q.ALGO_TCGEN05):
+        base = Problem(q, w, q.KV_BF16, algo=algo)
+        cast_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for _ in range(args.warmup):
+            q.kv_pool_cast_bf16(w.pool_fp8, base.data)
+            base.step()
+        torch.cuda.synchronize()
+        for k in range(steps):
+            cast_ev[k][0].record()
+            q.kv_pool_cast_bf16(w.pool_fp8, base.data)
+            cast_ev[k][1].record()
+            dec_ev[k][0].record()
+            base.step()
+            dec_ev[k][1].record()
+        torch.cuda.synchronize()
+        c_ms = float(np.mean([a.elapsed_time(b) for a, b in cast_ev]))
+        d_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
+        if best is None or c_ms + d_ms < best[0] + best[1]:
+            best = (c_ms, d_ms, "tcgen05" if algo == q.ALGO_TCGEN05 else "mma_sync")
+        del base
+        torch.cuda.empty_cache()
+    cast_ms, bdec_ms, bdec_algo = best
+    # gather-then-cast: only the batch's pages cast into a compact BF16 pool, read with ids 0..n-1
+    ids = torch.from_numpy(w.kv_indices).to(dev)
+    n_act = int(w.kv_indices.size)
+    compact = dataclasses.replace(w, kv_indices=np.arange(n_act, dtype=np.int32), num_pages=n_act)
+    gbest = None
+    for algo in (q.ALGO_MMA_SYNC, q.ALGO_TCGEN05):
+        gb = Problem(q, compact, q.KV_BF16, algo=algo)
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for _ in range(args.warmup):
+            q.kv_gather_pages_bf16(w.pool_fp8, ids, gb.data)
+            gb.step()
+        torch.cuda.synchronize()
+        for e0, e1, e2 in gev:
+            e0.record()
+            q.kv_gather_pages_bf16(w.pool_fp8, ids, gb.data)
+            e1.record()
+            gb.step()
+            e2.record()
+        torch.cuda.synchronize()
+        g_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in gev]))
+        d_ms = float(np.mean([b.elapsed_time(c) for _, b, c in gev]))
+        if gbest is None or g_ms + d_ms < gbest[0] + gbest[1]:
+            gbest = (g_ms, d_ms, "tcgen05" if algo == q.ALGO_TCGEN05 else "mma_sync")
+        del gb
+        torch.cuda.empty_cache()
     pool_bytes = w.num_pages * 64 * LATENT
     r["cast_then_attend"] = {
         "cast_us": round(cast_ms * 1e3, 2), "cast_bytes": 3 * pool_bytes,
         "cast_gbs": round(3 * pool_bytes / (cast_ms * 1e-3) / 1e9, 1),
-        "bf16_decode_us": round(bdec_ms * 1e3, 2),
+        "bf16_decode_us": round(bdec_ms * 1e3, 2), "bf16_decode_kernel": bdec_algo,
         "us_per_layer": round((cast_ms + bdec_ms) * 1e3, 2),
         "ms_per_78_layers": round(78 * (cast_ms + bdec_ms), 3)}
+    gmoved = n_act * 64 * LATENT * 3
+    r["gather_then_cast"] = {
+        "active_pages": n_act, "pool_pages": w.num_pages,
+        "gather_cast_us": round(gbest[0] * 1e3, 2), "gather_cast_bytes": gmoved,
+        "gather_cast_gbs": round(gmoved / (gbest[0] * 1e-3) / 1e9, 1),
+        "bf16_decode_us": round(gbest[1] * 1e3, 2), "bf16_decode_kernel": gbest[2],
+        "us_per_layer": round((gbest[0] + gbest[1]) * 1e3, 2),
+        "ms_per_78_layers": round(78 * (gbest[0] + gbest[1]), 3),
+        "speedup_vs_cast_then_attend": round((cast_ms + bdec_ms) / (gbest[0] + gbest[1]), 3)}
     r["fused_ms_per_78_layers"] = round(78 * ms, 3)
+    r["speedup_vs_gather_then_cast"] = round((gbest[0] + gbest[1]) / ms, 2)
     r["speedup_vs_cast_then_attend"] = round((cast_ms + bdec_ms) / ms, 2)
     res["mla_fp8_mixed_b64_h128_pool495552"] = r
     return res

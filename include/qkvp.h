@@ -241,6 +241,48 @@ int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* kv_len_host
 int kv_pool_cast_bf16(const uint8_t* in, int64_t n_elems, void* out, qkvp_stream_t stream);
 
 /*
+ * kv_gather_fp8 - the extend path's gather: each request's cached tokens into one contiguous FP8
+ * E4M3 workspace, the buffer a chunked-prefill step attends over and that every layer reuses.
+ * Source: "SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "SGLang implementation", item 2 (the
+ * cached prefix is gathered and dequantized into an FP8 workspace shared across layers, then joined
+ * with the current chunk's KV for FP8 attention).
+ *   Workspace row tok_indptr[r] + t (t < tok_indptr[r+1] - tok_indptr[r]) is token t of request r,
+ *   read from page kv_indices[kv_indptr[r] + t / 64], offset t % 64.
+ *   FP8 pool: the bytes are copied. NVFP4 pool: element i becomes E4M3_RNE_satfinite(v) with
+ *   v = fp32(scale(block) * e2m1(code)) * global_scale (the first product is exact; the second is one
+ *   FP32 rounding): the workspace holds the E4M3 domain the cache was quantized from. The page does
+ *   not say how the workspace is scaled; this is the plain reading.
+ *  kv_data, kv_scale  device pool as for mla_decode_run (kv_scale NULL for FP8); 16-byte aligned.
+ *  kv_dtype           QKVP_KV_FP8_E4M3 or QKVP_KV_NVFP4; global_scale 1 for FP8, finite > 0 for NVFP4.
+ *  kv_indptr          device int32 [batch + 1] (pages); kv_indices device int32 [nnz] page ids.
+ *  tok_indptr         device int64 [batch + 1], non-decreasing, tok_indptr[0] = 0,
+ *                     tok_indptr[batch] = total_tokens (the caller's contract; rows are matched to
+ *                     requests by binary search over it).
+ *  out                device uint8 [total_tokens][576], 16-byte aligned; every row is written.
+ * Every table entry is bounds-checked on the device: a row whose entry lies outside the request's
+ * pages, the table (nnz) or the pool (num_pages) is written as zeros. Errors: QKVP_E_INVALID for
+ * bad arguments, QKVP_E_UNSUPPORTED for page_size != 64 or a BF16 pool.
+ */
+int kv_gather_fp8(const void* kv_data, const uint8_t* kv_scale, int32_t kv_dtype, float global_scale,
+                  int32_t page_size, int64_t num_pages, const int32_t* kv_indptr, const int32_t* kv_indices,
+                  int64_t nnz, const int64_t* tok_indptr, int32_t batch, int64_t total_tokens, uint8_t* out,
+                  qkvp_stream_t stream);
+
+/*
+ * kv_gather_pages_bf16 - the gather-then-cast baseline: only the pages a batch reads, cast to BF16
+ * into a compact pool that a BF16 decode then reads with page ids 0..n_pages-1. Source: "The FP8 KV
+ * Cache Wall", sections "The Message" and "Aftermath" (Option B: cast only the active tokens, not
+ * the whole pool; measured there at +29%). Used only to measure that baseline.
+ *  kv_data   device FP8 pool [num_pages][64][576], 16-byte aligned.
+ *  page_ids  device int32 [n_pages]; out device BF16 [n_pages][64][576], 16-byte aligned.
+ * Page i of out is pool page page_ids[i] cast exactly (NaN bytes become 0x7FC0); an id outside the
+ * pool gives a zero page. Errors: QKVP_E_INVALID for bad arguments, QKVP_E_UNSUPPORTED for
+ * page_size != 64.
+ */
+int kv_gather_pages_bf16(const uint8_t* kv_data, int32_t page_size, int64_t num_pages, const int32_t* page_ids,
+                         int64_t n_pages, void* out, qkvp_stream_t stream);
+
+/*
  * qkvp_encode_f32 - the device rounding routines of kv_append_quant applied to raw FP32 values:
  * fmt 1 -> E4M3 (nearest even, saturating at +-448, NaN -> 0x7F); fmt 2 -> E2M1 (nearest even,
  * saturating at +-6, NaN -> 0x0). One code byte per input. Exposed so the rounding can be checked

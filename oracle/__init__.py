@@ -81,6 +81,11 @@ def lib():
                                        c.c_void_p]
             L.qo_cast_fp8_to_bf16.restype = None
             L.qo_cast_fp8_to_bf16.argtypes = [c.c_void_p, c.c_int64, c.c_void_p]
+            L.qo_gather_fp8.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_float, c.c_int, c.c_int64,
+                                        c.c_void_p, c.c_void_p, c.c_int64, c.c_void_p, c.c_int, c.c_void_p]
+            L.qo_gather_fp8.restype = c.c_int64
+            L.qo_gather_pages_bf16.argtypes = [c.c_void_p, c.c_int, c.c_int64, c.c_void_p, c.c_int64,
+                                               c.c_void_p]
             L.qo_hardware_threads.restype = c.c_int
             _lib = L
     return _lib
@@ -220,4 +225,28 @@ def cast_fp8_to_bf16(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.uint8)
     out = np.empty(x.shape, dtype=np.uint16)
     lib().qo_cast_fp8_to_bf16(_p(x), x.size, _p(out))
+    return out
+
+
+def gather_fp8(kv_data: np.ndarray, kv_scale, kv_dtype: int, g: float, page_size: int, num_pages: int,
+               kv_indptr, kv_indices, tok_indptr):
+    """c7: gather each request's tokens into a contiguous E4M3 workspace [tok_indptr[-1], 576]
+    (FP8 copied, NVFP4 dequantized and re-encoded). Returns (workspace, rows from bad page ids)."""
+    kv_indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
+    kv_indices = np.ascontiguousarray(kv_indices, dtype=np.int32)
+    tok_indptr = np.ascontiguousarray(tok_indptr, dtype=np.int64)
+    out = np.empty((int(tok_indptr[-1]), D_LATENT), dtype=np.uint8)
+    ps = _p(np.ascontiguousarray(kv_scale)) if kv_scale is not None else None
+    bad = lib().qo_gather_fp8(_p(np.ascontiguousarray(kv_data)), ps, kv_dtype, float(np.float32(g)), page_size,
+                              num_pages, _p(kv_indptr), _p(kv_indices), kv_indices.size, _p(tok_indptr),
+                              len(tok_indptr) - 1, _p(out))
+    return out, int(bad)
+
+
+def gather_pages_bf16(pool: np.ndarray, page_ids, page_size: int = 64) -> np.ndarray:
+    """c8: pages page_ids of an FP8 pool [P, page_size, 576], cast to BF16 bits [n, page_size, 576]."""
+    pool = np.ascontiguousarray(pool, dtype=np.uint8)
+    ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+    out = np.empty((ids.size, page_size, D_LATENT), dtype=np.uint16)
+    lib().qo_gather_pages_bf16(_p(pool), page_size, pool.shape[0], _p(ids), ids.size, _p(out))
     return out

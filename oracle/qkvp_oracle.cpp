@@ -364,6 +364,68 @@ void qo_cast_fp8_to_bf16(const uint8_t* in, int64_t n, uint16_t* out) {
   }
 }
 
+// c7: the extend path's gather ("SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "SGLang
+// implementation", item 2: the cached prefix is gathered and dequantized into an FP8 workspace shared
+// by all layers). Row tok_indptr[r] + t of `out` ([tok_indptr[batch]][576] E4M3 bytes) holds token t
+// of request r, read from slot kv_indices[p] * page_size + t % page_size with
+// p = kv_indptr[r] + t / page_size. FP8 pools are copied byte for byte. NVFP4 elements become
+//   v = fp32(value(s8) * value(c)) * g   (the first product is exact, at most 4 + 2 significant
+//                                           bits; the multiply by g is one FP32 rounding)
+//   byte = E4M3_RNE_satfinite(v)         (c2)
+// which reads "dequantize into FP8" as a return to the E4M3 domain the NVFP4 data was quantized from
+// (the page gives no other scale for the workspace). A row whose page-table entry lies outside the
+// request's pages, the table (nnz entries) or the pool is written as zeros. Returns the number of
+// such rows.
+int64_t qo_gather_fp8(const void* kv_data, const uint8_t* kv_scale, int kv_dtype, float g, int page_size,
+                      int64_t num_pages, const int32_t* kv_indptr, const int32_t* kv_indices, int64_t nnz,
+                      const int64_t* tok_indptr, int batch, uint8_t* out) {
+  int64_t bad = 0;
+  for (int r = 0; r < batch; ++r) {
+    for (int64_t t = 0; t < tok_indptr[r + 1] - tok_indptr[r]; ++t) {
+      uint8_t* row = out + (tok_indptr[r] + t) * kLatent;
+      const int64_t p = kv_indptr[r] + t / page_size;
+      const bool ok_p = p < kv_indptr[r + 1] && p >= 0 && p < nnz;
+      const int64_t page = ok_p ? kv_indices[p] : -1;
+      if (page < 0 || page >= num_pages) {
+        std::memset(row, 0, kLatent);
+        ++bad;
+        continue;
+      }
+      const int64_t slot = page * page_size + t % page_size;
+      for (int i = 0; i < kLatent; ++i) {
+        if (kv_dtype == KV_FP8) {
+          row[i] = static_cast<const uint8_t*>(kv_data)[slot * kLatent + i];
+        } else {
+          const uint8_t byte = static_cast<const uint8_t*>(kv_data)[slot * kPackedPerToken + i / 2];
+          const uint8_t code = (i & 1) ? (byte >> 4) : (byte & 0xF);
+          const float se = static_cast<float>(e4m3_value(kv_scale[slot * kBlocksPerToken + i / kBlock]) *
+                                              e2m1_value(code));
+          const float v = se * g;
+          row[i] = e4m3_encode(v);
+        }
+      }
+    }
+  }
+  return bad;
+}
+
+// c8: the gather-then-cast baseline ("The FP8 KV Cache Wall", sections "The Message" and
+// "Aftermath": Option B, cast only the active tokens instead of the whole pool): page i of `out`
+// ([n][page_size][576] BF16 bits) is pool page page_ids[i] cast
+// exactly as in the pool-wide cast (NaN bytes become 0x7FC0). Page ids outside the pool give zeros.
+void qo_gather_pages_bf16(const uint8_t* pool, int page_size, int64_t num_pages, const int32_t* page_ids,
+                          int64_t n, uint16_t* out) {
+  const int64_t per = static_cast<int64_t>(page_size) * kLatent;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t page = page_ids[i];
+    if (page < 0 || page >= num_pages) {
+      std::memset(out + i * per, 0, per * sizeof(uint16_t));
+      continue;
+    }
+    qo_cast_fp8_to_bf16(pool + page * per, per, out + i * per);
+  }
+}
+
 int qo_hardware_threads() { return static_cast<int>(std::thread::hardware_concurrency()); }
 
 }  // extern "C"

@@ -23,8 +23,8 @@ ALGO_AUTO, ALGO_MMA_SYNC, ALGO_TCGEN05 = 0, 1, 2
 LATENT_DIM, V_DIM, PAGE_SIZE = 576, 512, 64
 
 EXPORTS = ["kv_append_quant", "mla_decode_plan", "mla_decode_run", "mla_decode_attend",
-           "mla_decode_combine", "mla_decode_noalloc", "kv_pool_cast_bf16",
-           "qkvp_encode_f32", "qkvp_status_string", "qkvp_version"]
+           "mla_decode_combine", "mla_decode_noalloc", "kv_pool_cast_bf16", "kv_gather_fp8",
+           "kv_gather_pages_bf16", "qkvp_encode_f32", "qkvp_status_string", "qkvp_version"]
 
 
 class qkvp_plan(ctypes.Structure):
@@ -73,12 +73,14 @@ def load(path: str | None = None):
         L.mla_decode_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i64, vp, f32,
                                          f32, vp, vp, vp]
         L.kv_pool_cast_bf16.argtypes = [vp, i64, vp, vp]
+        L.kv_gather_fp8.argtypes = [vp, vp, i32, f32, i32, i64, vp, vp, i64, vp, i32, i64, vp, vp]
+        L.kv_gather_pages_bf16.argtypes = [vp, i32, i64, vp, i64, vp, vp]
         L.qkvp_encode_f32.argtypes = [vp, i64, i32, vp, vp]
         L.qkvp_status_string.restype = c.c_char_p
         L.qkvp_status_string.argtypes = [c.c_int]
         for fn in ("kv_append_quant", "mla_decode_plan", "mla_decode_run", "mla_decode_attend",
-                   "mla_decode_combine", "mla_decode_noalloc", "kv_pool_cast_bf16",
-                   "qkvp_encode_f32", "qkvp_version"):
+                   "mla_decode_combine", "mla_decode_noalloc", "kv_pool_cast_bf16", "kv_gather_fp8",
+                   "kv_gather_pages_bf16", "qkvp_encode_f32", "qkvp_version"):
             getattr(L, fn).restype = c.c_int
         _lib = L
         return L
@@ -193,6 +195,30 @@ def kv_pool_cast_bf16(src, out, stream=None, raise_on_error: bool = True) -> int
     """The cast-then-attend baseline's pool-wide FP8 -> BF16 cast."""
     st = load().kv_pool_cast_bf16(_ptr(src), int(src.numel()), _ptr(out), _stream(stream))
     return _check("kv_pool_cast_bf16", st, raise_on_error)
+
+
+def kv_gather_fp8(kv_data, kv_scale, kv_dtype: int, global_scale: float, kv_indptr, kv_indices, tok_indptr,
+                  out, num_pages: int | None = None, page_size: int = PAGE_SIZE, stream=None,
+                  raise_on_error: bool = True) -> int:
+    """Extend-path gather of each request's tokens into the FP8 workspace out [T, 576] (see qkvp.h).
+    kv_indptr / kv_indices int32 and tok_indptr int64 are device tensors."""
+    if num_pages is None:
+        num_pages = int(kv_data.shape[0])
+    batch = int(tok_indptr.shape[0]) - 1
+    st = load().kv_gather_fp8(_ptr(kv_data), _ptr(kv_scale), kv_dtype, float(global_scale), page_size,
+                              int(num_pages), _ptr(kv_indptr), _ptr(kv_indices), int(kv_indices.numel()),
+                              _ptr(tok_indptr), batch, int(out.shape[0]), _ptr(out), _stream(stream))
+    return _check("kv_gather_fp8", st, raise_on_error)
+
+
+def kv_gather_pages_bf16(kv_data, page_ids, out, num_pages: int | None = None, page_size: int = PAGE_SIZE,
+                         stream=None, raise_on_error: bool = True) -> int:
+    """Gather-then-cast baseline: pool pages page_ids (device int32) cast into out [n, 64, 576] BF16."""
+    if num_pages is None:
+        num_pages = int(kv_data.shape[0])
+    st = load().kv_gather_pages_bf16(_ptr(kv_data), page_size, int(num_pages), _ptr(page_ids),
+                                     int(page_ids.numel()), _ptr(out), _stream(stream))
+    return _check("kv_gather_pages_bf16", st, raise_on_error)
 
 
 def qkvp_encode_f32(x, fmt: int, codes, stream=None, raise_on_error: bool = True) -> int:

@@ -311,6 +311,54 @@ int mla_decode_run(const qkvp_plan* plan, const void* q, const void* kv_data, co
   return mla_decode_combine(plan, global_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
+int kv_gather_fp8(const void* kv_data, const uint8_t* kv_scale, int32_t kv_dtype, float global_scale,
+                  int32_t page_size, int64_t num_pages, const int32_t* kv_indptr, const int32_t* kv_indices,
+                  int64_t nnz, const int64_t* tok_indptr, int32_t batch, int64_t total_tokens, uint8_t* out,
+                  qkvp_stream_t stream) {
+  if (page_size != kPage) return QKVP_E_UNSUPPORTED;
+  if (kv_dtype == QKVP_KV_BF16) return QKVP_E_UNSUPPORTED;
+  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4) return QKVP_E_INVALID;
+  if (batch < 0 || total_tokens < 0 || nnz < 0 || num_pages < 0) return QKVP_E_INVALID;
+  if (kv_dtype == QKVP_KV_NVFP4) {
+    if (!finite_float(global_scale) || !(global_scale > 0.0f)) return QKVP_E_INVALID;
+  } else if (global_scale != 1.0f || kv_scale) {
+    return QKVP_E_INVALID;
+  }
+  if (batch == 0 || total_tokens == 0) return QKVP_OK;
+  if (!kv_data || !kv_indptr || !kv_indices || !tok_indptr || !out) return QKVP_E_INVALID;
+  if (!aligned(kv_data, 16) || !aligned(out, 16) || !aligned(tok_indptr, 8) || !aligned(kv_indptr, 4) ||
+      !aligned(kv_indices, 4))
+    return QKVP_E_INVALID;
+  if (kv_dtype == QKVP_KV_NVFP4 && !kv_scale) return QKVP_E_INVALID;
+  GatherArgs a{};
+  a.kv = static_cast<const uint8_t*>(kv_data);
+  a.kv_scale = kv_scale;
+  a.num_pages = num_pages;
+  a.kv_indptr = kv_indptr;
+  a.kv_indices = kv_indices;
+  a.nnz = nnz;
+  a.tok_indptr = tok_indptr;
+  a.out = out;
+  a.total_tokens = total_tokens;
+  a.batch = batch;
+  a.kv_dtype = kv_dtype == QKVP_KV_NVFP4 ? KV_NVFP4 : KV_FP8;
+  a.g = global_scale;
+  cudaError_t e = launch_gather_fp8(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
+}
+
+int kv_gather_pages_bf16(const uint8_t* kv_data, int32_t page_size, int64_t num_pages, const int32_t* page_ids,
+                         int64_t n_pages, void* out, qkvp_stream_t stream) {
+  if (page_size != kPage) return QKVP_E_UNSUPPORTED;
+  if (n_pages < 0 || num_pages < 0) return QKVP_E_INVALID;
+  if (n_pages == 0) return QKVP_OK;
+  if (!kv_data || !page_ids || !out || !aligned(kv_data, 16) || !aligned(out, 16) || !aligned(page_ids, 4))
+    return QKVP_E_INVALID;
+  cudaError_t e = launch_gather_pages_bf16(kv_data, num_pages, page_ids, n_pages, out,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
+}
+
 int kv_pool_cast_bf16(const uint8_t* in, int64_t n_elems, void* out, qkvp_stream_t stream) {
   if (n_elems < 0 || n_elems % 16) return QKVP_E_INVALID;
   if (n_elems == 0) return QKVP_OK;

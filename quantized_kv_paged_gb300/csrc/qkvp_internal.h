@@ -72,6 +72,24 @@ inline TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch
   return t;
 }
 
+// Arguments of the extend-path gather (kv_gather_fp8).
+struct GatherArgs {
+  const uint8_t* kv;
+  const uint8_t* kv_scale;
+  int64_t num_pages;
+  const int32_t* kv_indptr;   // [batch + 1], pages
+  const int32_t* kv_indices;  // [nnz] page ids
+  int64_t nnz;
+  const int64_t* tok_indptr;  // [batch + 1], workspace rows
+  uint8_t* out;               // [total_tokens][576] E4M3
+  int64_t total_tokens;
+  int batch, kv_dtype;
+  float g;
+};
+
+cudaError_t launch_gather_fp8(const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_gather_pages_bf16(const uint8_t* pool, int64_t num_pages, const int32_t* ids, int64_t n,
+                                     void* out, cudaStream_t s);
 cudaError_t launch_append(const void* src, int src_dtype, int64_t n, const int64_t* slots,
                           void* kv_data, uint8_t* kv_scale, int kv_dtype, float g,
                           int64_t num_slots, cudaStream_t s);

@@ -128,3 +128,33 @@ def test_run_and_append_reject_before_launch(lib):
     assert st == q.QKVP_E_INVALID
     assert lib.kv_pool_cast_bf16(16, 17, 16, None) == q.QKVP_E_INVALID
     assert lib.qkvp_encode_f32(16, 4, 3, 16, None) == q.QKVP_E_INVALID
+
+
+def test_gather_entry_points_reject_before_launch(lib):
+    f = lib.kv_gather_fp8
+    ok = dict(kv=16, sc=16, dt=2, g=1.0, ps=64, np_=10, ip=16, ix=16, nnz=4, tok=16, b=2, t=100, out=16)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["kv"], a["sc"], a["dt"], a["g"], a["ps"], a["np_"], a["ip"], a["ix"], a["nnz"], a["tok"],
+                 a["b"], a["t"], a["out"], None)
+    assert call(ps=32) == q.QKVP_E_UNSUPPORTED
+    assert call(dt=3) == q.QKVP_E_UNSUPPORTED                 # BF16 pool
+    assert call(dt=7) == q.QKVP_E_INVALID
+    assert call(g=0.0) == q.QKVP_E_INVALID
+    assert call(g=float("inf")) == q.QKVP_E_INVALID
+    assert call(dt=1) == q.QKVP_E_INVALID                     # FP8 with a scale pool
+    assert call(dt=1, sc=None, g=2.0) == q.QKVP_E_INVALID     # FP8 with g != 1
+    assert call(sc=None) == q.QKVP_E_INVALID                  # NVFP4 without scales
+    assert call(b=-1) == q.QKVP_E_INVALID
+    assert call(t=-5) == q.QKVP_E_INVALID
+    assert call(out=None) == q.QKVP_E_INVALID
+    assert call(out=24) == q.QKVP_E_INVALID                   # output not 16-byte aligned
+    assert call(tok=20) == q.QKVP_E_INVALID                   # tok_indptr not 8-byte aligned
+    assert call(t=0) == q.QKVP_OK and call(b=0) == q.QKVP_OK  # nothing to do
+    g = lib.kv_gather_pages_bf16
+    assert g(16, 32, 10, 16, 3, 16, None) == q.QKVP_E_UNSUPPORTED
+    assert g(16, 64, 10, 16, -1, 16, None) == q.QKVP_E_INVALID
+    assert g(16, 64, 10, 16, 0, 16, None) == q.QKVP_OK
+    assert g(None, 64, 10, 16, 3, 16, None) == q.QKVP_E_INVALID
+    assert g(16, 64, 10, 16, 3, 8, None) == q.QKVP_E_INVALID
