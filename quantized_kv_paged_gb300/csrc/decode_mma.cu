@@ -28,6 +28,7 @@
 
 #include "qkvp_device.cuh"
 #include "qkvp_internal.h"
+#include "tc_ptx.cuh"
 
 namespace qkvp {
 namespace {
@@ -40,9 +41,40 @@ constexpr int raw_bytes() {
   return KV == KV_FP8 ? kPage * kLatent : (KV == KV_NVFP4 ? kPage * (kPacked + kScales) : 0);
 }
 
+constexpr int kNT = 256;                   // threads per CTA: every warp dequantizes
+
+// MMA warp pairs of a CTA with HC heads (see the token groups in the kernel).
+template <int HC>
+constexpr int pairs() { return (HC / 16) * ((HC / 16) >= 3 ? 1 : 4 / (HC / 16)); }
+
+// Raw page buffers: two (pages fetched two ahead) unless that overflows shared memory (64 heads).
+template <int KV, int HC>
+constexpr int raw_bufs() {
+  return KV == KV_BF16 ? 0 : (HC * kRowBytes + kPage * kRowBytes + 2 * raw_bytes<KV>() + pairs<HC>() * 8192 + 64 <= 232448 - 1024 ? 2 : 1);
+}
+
 template <int KV, int HC>
 constexpr int smem_bytes() {
-  return HC * kRowBytes + kPage * kRowBytes + raw_bytes<KV>() + (HC / 16) * 2 * 32 * 32 * 4 + 16;
+  return HC * kRowBytes + kPage * kRowBytes + raw_bufs<KV, HC>() * raw_bytes<KV>() + pairs<HC>() * 2 * 32 * 32 * 4 + 64;
+}
+
+// Raw bytes of one page (FP8: the page; NVFP4: data then block scales) into a raw buffer with bulk
+// asynchronous copies, counted on `bar` (one expect-tx arrival by the issuing thread). A page id
+// outside the pool copies nothing; the arrival alone completes the phase and the page reads as empty.
+template <int KV>
+__device__ __forceinline__ void fetch_page(const DecodeArgs& a, int64_t page, uint32_t s_raw, uint32_t bar) {
+  if (page < 0 || page >= a.num_pages) {
+    tc::mbar_arrive(bar);
+    return;
+  }
+  if (KV == KV_FP8) {
+    tc::mbar_arrive_expect_tx(bar, kPage * kLatent);
+    tc::bulk_load(s_raw, a.kv + page * (kPage * kLatent), kPage * kLatent, bar);
+  } else {
+    tc::mbar_arrive_expect_tx(bar, kPage * (kPacked + kScales));
+    tc::bulk_load(s_raw, a.kv + page * (kPage * kPacked), kPage * kPacked, bar);
+    tc::bulk_load(s_raw + kPage * kPacked, a.kv_scale + page * (kPage * kScales), kPage * kScales, bar);
+  }
 }
 
 // Fetch the raw bytes of one page (or, for BF16, the page itself) with cp.async.
@@ -126,30 +158,51 @@ __device__ __forceinline__ void dequant_page(const uint8_t* s_raw, uint8_t* s_kv
 }
 
 template <int KV, int HC>
-__global__ void __launch_bounds__(HC * 4, 1) decode_mma_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) {
   constexpr int NG = HC / 16;       // 16-head groups in this CTA
-  constexpr int NT = NG * 64;       // two warps per group
+  // With few heads the page's 64 tokens are split among warp pairs too, so that all 8 warps do
+  // math: TG token groups of TPG tokens, each pair with its own softmax state, merged at the end
+  // of a segment. 16 heads: 4 x 16 tokens; 32: 2 x 32; 48 and 64: 1 x 64.
+  constexpr int TG = NG >= 3 ? 1 : 4 / NG;
+  constexpr int NPAIR = NG * TG;
+  constexpr int TPG = kPage / TG;
+  constexpr int NP = TPG / 16;      // 16-token tiles per token group
+  constexpr int NT = kNT;
+  constexpr int NB = raw_bufs<KV, HC>();
+  constexpr int NBx = NB > 0 ? NB : 1;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_q = smem;
   uint8_t* s_kv = s_q + HC * kRowBytes;
   uint8_t* s_raw = s_kv + kPage * kRowBytes;
-  float* s_x = reinterpret_cast<float*>(s_raw + raw_bytes<KV>());
-  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + (HC / 16) * 2 * 1024);
+  float* s_x = reinterpret_cast<float*>(s_raw + NB * raw_bytes<KV>());
+  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + NPAIR * 2 * 1024);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_qmax + 2);          // NB FULL barriers (8-byte aligned)
   const uint32_t a_q = dev::smem_u32(s_q), a_kv = dev::smem_u32(s_kv), a_raw = dev::smem_u32(s_raw);
+  const uint32_t a_bar = dev::smem_u32(s_bar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int grp = warp >> 1, half = warp & 1;
+  const int pi = warp >> 1, half = warp & 1;
+  const int grp = pi % NG, tg = pi / NG;  // head group and token group of this warp's pair
+  const int t0 = tg * TPG;                // first token of the page this pair attends
   const int g8 = lane >> 2, t4 = lane & 3;
   const int worker = blockIdx.x / a.ctas_per_worker;
   const int h0 = (blockIdx.x % a.ctas_per_worker) * HC;
   const int seg_b = a.worker_ptr[worker], seg_e = a.worker_ptr[worker + 1];
+  const bool mma_warp = warp < 2 * NPAIR;
+  if (KV != KV_BF16 && tid == 0) {
+    for (int b = 0; b < NB; ++b) tc::mbar_init(a_bar + 8 * b, 1);
+    tc::fence_mbar_init();
+  }
+  int fills[NBx];                   // completed phases of each raw buffer's barrier
+#pragma unroll
+  for (int b = 0; b < NBx; ++b) fills[b] = 0;
 
   // ldmatrix lane addresses (bytes, relative to the tile bases)
   const uint32_t q_lane = ((grp * 16 + (lane & 15)) * kRow + (lane >> 4) * 8) * 2;
   const uint32_t k_lane = (((lane & 7) + ((lane >> 4) << 3)) * kRow + ((lane >> 3) & 1) * 8) * 2;
   const uint32_t v_lane = (((lane & 7) + ((lane >> 3) & 1) * 8) * kRow + half * 256 + (lane >> 4) * 8) * 2;
-  float* x_mine = s_x + (grp * 2 + half) * 1024;
-  float* x_peer = s_x + (grp * 2 + (half ^ 1)) * 1024;
+  float* x_mine = s_x + (pi * 2 + half) * 1024;
+  float* x_peer = s_x + (pi * 2 + (half ^ 1)) * 1024;
 
   int cur_req = -1;
   float q_scale_log2 = a.scale_log2;
@@ -199,47 +252,62 @@ __global__ void __launch_bounds__(HC * 4, 1) decode_mma_kernel(const DecodeArgs 
     for (int i = 0; i < 32; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.0f, 0.0f};
 
+    // raw pages of this segment stream in NB ahead of the page being dequantized
+    if (KV != KV_BF16 && tid == 0) {
+      for (int k = 0; k < NB && k < seg.num_pages; ++k)
+        fetch_page<KV>(a, a.kv_indices[seg.page_begin + k], a_raw + k * raw_bytes<KV>(), a_bar + 8 * k);
+    }
     int64_t page = a.kv_indices[seg.page_begin];
-    if (KV != KV_BF16) issue_page<KV, NT>(a, page, min(kPage, seg.num_tokens), a_raw, a_kv, tid);
     for (int j = 0; j < seg.num_pages; ++j) {
       const int valid = min(kPage, seg.num_tokens - j * kPage);
       const bool page_ok = page >= 0 && page < a.num_pages;
-      if (KV == KV_BF16) issue_page<KV, NT>(a, page, valid, a_raw, a_kv, tid);
-      dev::cp_async_wait_all();
+      const int buf = NB > 0 ? j % NB : 0;
+      if (KV == KV_BF16) {
+        issue_page<KV, NT>(a, page, valid, a_raw, a_kv, tid);
+        dev::cp_async_wait_all();
+      } else {
+        // bounded wait: a timeout sets a status bit, and the page then reads as whatever is there
+        if (!tc::mbar_wait(a_bar + 8 * buf, fills[buf] & 1)) {
+          if (lane == 0) atomicOr(a.status, 16);
+        }
+        ++fills[buf];
+      }
       __syncthreads();
-      dequant_page<KV, NT>(s_raw, s_kv, page_ok ? valid : 0, tid);
+      dequant_page<KV, NT>(s_raw + buf * raw_bytes<KV>(), s_kv, page_ok ? valid : 0, tid);
       __syncthreads();
-      if (j + 1 < seg.num_pages) {
-        page = a.kv_indices[seg.page_begin + j + 1];
-        if (KV != KV_BF16) issue_page<KV, NT>(a, page, min(kPage, seg.num_tokens - (j + 1) * kPage), a_raw, a_kv, tid);
+      if (j + 1 < seg.num_pages) page = a.kv_indices[seg.page_begin + j + 1];
+      if (KV != KV_BF16 && tid == 0 && j + NB < seg.num_pages) {
+        tc::fence_proxy_async_smem();   // this buffer's reads are done before the copy refills it
+        fetch_page<KV>(a, a.kv_indices[seg.page_begin + j + NB], a_raw + buf * raw_bytes<KV>(), a_bar + 8 * buf);
       }
       const int live = page_ok ? valid : 0;
+      if (mma_warp) {
 
-      // ---- S partial = Q[:, my dims] K[:, my dims]^T  (16 heads x 64 tokens) ----
-      float s[8][4];
+      // ---- S partial = Q[:, my dims] K[my tokens, my dims]^T  (16 heads x TPG tokens) ----
+      float s[2 * NP][4];
 #pragma unroll
-      for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
+      for (int n = 0; n < 2 * NP; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
 #pragma unroll 2
       for (int ks = 0; ks < 18; ++ks) {
         const int kk = half * 288 + ks * 16;
         uint32_t a0, a1, a2, a3;
         dev::ldsm_x4(a_q + q_lane + kk * 2, a0, a1, a2, a3);
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
+        for (int p = 0; p < NP; ++p) {
           uint32_t b0, b1, b2, b3;
-          dev::ldsm_x4(a_kv + k_lane + (p * 16 * kRow + kk) * 2, b0, b1, b2, b3);
+          dev::ldsm_x4(a_kv + k_lane + ((t0 + p * 16) * kRow + kk) * 2, b0, b1, b2, b3);
           dev::mma_f16(s[2 * p], a0, a1, a2, a3, b0, b1);
           dev::mma_f16(s[2 * p + 1], a0, a1, a2, a3, b2, b3);
         }
       }
       // ---- exchange the partial logits with the peer warp; sum in a fixed order ----
 #pragma unroll
-      for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) x_mine[(n * 4 + i) * 32 + lane] = s[n][i];
-      dev::named_bar_sync(1 + grp, 64);
+      dev::named_bar_sync(1 + pi, 64);
 #pragma unroll
-      for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float peer = x_peer[(n * 4 + i) * 32 + lane];
@@ -248,10 +316,10 @@ __global__ void __launch_bounds__(HC * 4, 1) decode_mma_kernel(const DecodeArgs 
       // ---- online softmax in base 2 (rows g8 and g8 + 8 of the 16 heads) ----
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int tok = n * 8 + 2 * t4 + (i & 1);
+          const int tok = t0 + n * 8 + 2 * t4 + (i & 1);
           const float v = tok < live ? s[n][i] * q_scale_log2 : -INFINITY;
           s[n][i] = v;
           mx[i >> 1] = fmaxf(mx[i >> 1], v);
@@ -268,7 +336,7 @@ __global__ void __launch_bounds__(HC * 4, 1) decode_mma_kernel(const DecodeArgs 
         l_r[r] *= alpha[r];
       }
 #pragma unroll
-      for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float p = dev::fast_exp2(s[n][i] - mref[i >> 1]);
@@ -282,7 +350,7 @@ __global__ void __launch_bounds__(HC * 4, 1) decode_mma_kernel(const DecodeArgs 
       }
       // ---- O[:, my 256 dims] += P V ----
 #pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
+      for (int kt = 0; kt < NP; ++kt) {
         const uint32_t pa0 = dev::pack_f16x2(s[2 * kt][0], s[2 * kt][1]);
         const uint32_t pa1 = dev::pack_f16x2(s[2 * kt][2], s[2 * kt][3]);
         const uint32_t pa2 = dev::pack_f16x2(s[2 * kt + 1][0], s[2 * kt + 1][1]);
@@ -290,19 +358,66 @@ __global__ void __launch_bounds__(HC * 4, 1) decode_mma_kernel(const DecodeArgs 
 #pragma unroll
         for (int vp = 0; vp < 16; ++vp) {
           uint32_t b0, b1, b2, b3;
-          dev::ldsm_x4_t(a_kv + v_lane + (kt * 16 * kRow + vp * 16) * 2, b0, b1, b2, b3);
+          dev::ldsm_x4_t(a_kv + v_lane + ((t0 + kt * 16) * kRow + vp * 16) * 2, b0, b1, b2, b3);
           dev::mma_f16(o[2 * vp], pa0, pa1, pa2, pa3, b0, b1);
           dev::mma_f16(o[2 * vp + 1], pa0, pa1, pa2, pa3, b2, b3);
         }
       }
+      }
       __syncthreads();  // s_kv and the exchange buffers are reused by the next page
     }
+    if (!mma_warp) continue;
 
     // ---- epilogue: normalise; write the output directly or a split partial ----
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 1);
       l_r[r] += __shfl_xor_sync(0xffffffffu, l_r[r], 2);
+    }
+    if (TG > 1) {
+      // merge the token groups of each head group by their maxima, in group order, through the
+      // page tile and raw buffers (no page of this segment is read any more): pairs tg > 0 store
+      // (O, m, l) in their fragment order, the tg = 0 pair of the same heads reads them back
+      float* mrg = reinterpret_cast<float*>(s_kv);
+      constexpr int kSlot = 32 * 128 + 32 * 4;            // one warp's O fragments, then m and l
+      static_assert(NG * (TG - 1) * 2 * kSlot * 4 <= kPage * kRowBytes + NB * raw_bytes<KV>() + NPAIR * 8192,
+                    "merge slots fit in the page tile, raw buffers and exchange buffers");
+      auto slot = [&](int g, int t, int hf) { return mrg + ((g * (TG - 1) + (t - 1)) * 2 + hf) * kSlot; };
+      if (tg > 0) {
+        float* d = slot(grp, tg, half);
+#pragma unroll
+        for (int u = 0; u < 128; ++u) d[u * 32 + lane] = o[u >> 2][u & 3];
+        d[4096 + lane] = m_r[0]; d[4096 + 32 + lane] = m_r[1];
+        d[4096 + 64 + lane] = l_r[0]; d[4096 + 96 + lane] = l_r[1];
+      }
+      dev::named_bar_sync(15, 64 * NPAIR);
+      if (tg > 0) continue;
+      float mt[TG][2], f[TG][2];
+#pragma unroll
+      for (int t = 0; t < TG; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) mt[t][r] = t == 0 ? m_r[r] : slot(grp, t, half)[4096 + 32 * r + lane];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float mstar = mt[0][r];
+#pragma unroll
+        for (int t = 1; t < TG; ++t) mstar = fmaxf(mstar, mt[t][r]);
+        float lsum = 0.0f;
+#pragma unroll
+        for (int t = 0; t < TG; ++t) {
+          f[t][r] = mt[t][r] == -INFINITY ? 0.0f : dev::fast_exp2(mt[t][r] - mstar);
+          lsum += (t == 0 ? l_r[r] : slot(grp, t, half)[4096 + 64 + 32 * r + lane]) * f[t][r];
+        }
+        m_r[r] = mstar;
+        l_r[r] = lsum;
+      }
+#pragma unroll
+      for (int u = 0; u < 128; ++u) {
+        float v = o[u >> 2][u & 3] * f[0][(u & 3) >> 1];
+#pragma unroll
+        for (int t = 1; t < TG; ++t) v += slot(grp, t, half)[u * 32 + lane] * f[t][(u & 3) >> 1];
+        o[u >> 2][u & 3] = v;
+      }
     }
     const float inv[2] = {l_r[0] > 0.0f ? 1.0f / l_r[0] : 0.0f, l_r[1] > 0.0f ? 1.0f / l_r[1] : 0.0f};
     const float lse2[2] = {l_r[0] > 0.0f ? m_r[0] + __log2f(l_r[0]) : -INFINITY,
@@ -336,7 +451,7 @@ cudaError_t launch_kv_hc(const DecodeArgs& a, cudaStream_t s) {
     configured = true;
   }
   const unsigned grid = static_cast<unsigned>(a.num_workers * a.ctas_per_worker);
-  decode_mma_kernel<KV, HC><<<grid, HC * 4, smem, s>>>(a);
+  decode_mma_kernel<KV, HC><<<grid, kNT, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -128,6 +128,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                :: "r"(bar), "r"(bytes) : "memory");
 }
 
+// Asynchronous bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global
+// memory into this CTA's shared memory, counted in bytes on the local mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
 // Asynchronous bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
 // CTA's shared memory to the same offset in CTA `rank` of the cluster; completion is counted in
 // bytes on the mbarrier at offset `bar_local` of that CTA.
