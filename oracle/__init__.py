@@ -22,7 +22,8 @@ _OUT = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 _lock = threading.Lock()
 
-KV_FP8, KV_NVFP4, KV_BF16 = 1, 2, 3
+KV_FP8, KV_NVFP4, KV_BF16, KV_FP8_PT = 1, 2, 3, 4
+PAGE_BYTES_PT = 64 * (576 + 4)      # c9 page: 64 rows of E4M3 codes, then 64 FP32 token scales
 SRC_FP8, SRC_BF16 = 1, 2
 D_LATENT, D_V = 576, 512
 
@@ -147,12 +148,16 @@ def nvfp4_block(x16, g: float):
 def quant_tokens(src: np.ndarray, src_dtype: int, kv_dtype: int, g: float = 1.0):
     """Token-major quantisation. src: uint8 [n,576] (FP8) or uint16 [n,576] (BF16 bits).
 
-    Returns data [n,576] (FP8) or (data [n,288], scales [n,36]) (NVFP4)."""
+    Returns data [n,576] (FP8), (data [n,288], scales [n,36]) (NVFP4) or (codes [n,576], token
+    scales float32 [n]) (FP8_PT, c9)."""
     src = np.ascontiguousarray(src)
     n = src.shape[0]
     if kv_dtype == KV_FP8:
         data = np.empty((n, D_LATENT), dtype=np.uint8)
         scale = np.empty((1,), dtype=np.uint8)
+    elif kv_dtype == KV_FP8_PT:
+        data = np.empty((n, D_LATENT), dtype=np.uint8)
+        scale = np.empty((n,), dtype=np.float32)
     else:
         data = np.empty((n, D_LATENT // 2), dtype=np.uint8)
         scale = np.empty((n, D_LATENT // 16), dtype=np.uint8)
@@ -160,6 +165,11 @@ def quant_tokens(src: np.ndarray, src_dtype: int, kv_dtype: int, g: float = 1.0)
     if rc:
         raise ValueError(f"qo_quant_tokens rc={rc}")
     return data if kv_dtype == KV_FP8 else (data, scale)
+
+
+def pt_pool(num_pages: int) -> np.ndarray:
+    """An empty (all-zero) per-token-scaled FP8 pool of `num_pages` c9 pages."""
+    return np.zeros((num_pages, PAGE_BYTES_PT), dtype=np.uint8)
 
 
 def append(src: np.ndarray, src_dtype: int, slots: np.ndarray, kv_dtype: int, g: float,

@@ -16,6 +16,9 @@
 //    "SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "NVFP4 format: two-level scaling".
 //  * Quantize-on-write and in-kernel dequant for decode: same page, section "SGLang
 //    implementation", items 1-3.
+//  * Per-token-scaled FP8 pages (c9): each token's E4M3 elements with 4 scale bytes of their own,
+//    64 tokens per page: "The Precision Frontier: Implementing bf16 Index Keys ...", section "The
+//    Message: Planning the bf16-K Implementation".
 //  * Attention is softmax(sm_scale * q . k) v with K = the whole latent and V = its first 512 dims,
 //    the paged CSR page table of the pages' plan() call: "The Smoking Gun", section "What Message
 //    1408 Actually Reveals".
@@ -38,7 +41,12 @@ constexpr int kBlock = 16;     // NVFP4 values per E4M3 block scale
 constexpr int kBlocksPerToken = kLatent / kBlock;      // 36
 constexpr int kPackedPerToken = kLatent / 2;           // 288 bytes of E2M1 pairs
 
-enum { KV_FP8 = 1, KV_NVFP4 = 2, KV_BF16 = 3 };
+enum { KV_FP8 = 1, KV_NVFP4 = 2, KV_BF16 = 3, KV_FP8_PT = 4 };
+
+// Per-token-scaled FP8 pages (c9): page p holds kPagePT token rows of 576 E4M3 codes, then the
+// kPagePT FP32 token scales (little-endian), kPagePT * (576 + 4) = 37,120 bytes in all.
+constexpr int kPagePT = 64;
+constexpr int64_t kPageBytesPT = static_cast<int64_t>(kPagePT) * (kLatent + 4);
 enum { SRC_FP8 = 1, SRC_BF16 = 2 };
 
 // ---- c1: code -> value tables, from the bit layouts ------------------------------------------
@@ -144,6 +152,32 @@ void nvfp4_block(const float* x, float g, uint8_t* packed, uint8_t* scale) {
   *scale = s8;
 }
 
+// ---- c9: per-token-scaled FP8 of one token ---------------------------------------------------
+// The pages' indexer key cache stores each token's FP8 elements with 4 scale bytes of their own, in
+// a paged uint8 buffer [npages, page_bytes] with 64 tokens per page ("The Precision Frontier:
+// Implementing bf16 Index Keys ...", section "The Message: Planning the bf16-K Implementation":
+// 128 elements + 4 scale bytes = 132 bytes per token). Here the layout carries the 576-wide latent:
+// 576 + 4 bytes per token. The pages give no formula for the scale; the one here maps the token's
+// largest magnitude onto E4M3's largest finite value (448, c1). FP32 throughout, one rounding per
+// operation:
+//   amax  = max |x_i|                     (NaN if any x_i is NaN)
+//   sigma = amax / 448
+//   c_i   = E4M3(x_i / sigma)             (c2), or E4M3(x_i) (a signed zero) when sigma == 0
+// The value of element i is sigma * value(c_i).
+void pt_token(const float* x, uint8_t* codes, float* sigma) {
+  float amax = 0.0f;
+  bool nan = false;
+  for (int i = 0; i < kLatent; ++i) {
+    if (x[i] != x[i]) nan = true;
+    const float a = std::fabs(x[i]);
+    if (a > amax) amax = a;
+  }
+  if (nan) amax = NAN;
+  const float s = amax / 448.0f;
+  for (int i = 0; i < kLatent; ++i) codes[i] = (s == 0.0f) ? e4m3_encode(x[i]) : e4m3_encode(x[i] / s);
+  *sigma = s;
+}
+
 float bf16_to_float(uint16_t b) {
   uint32_t u = static_cast<uint32_t>(b) << 16;
   float f;
@@ -218,12 +252,20 @@ void qo_nvfp4_block(const float* x16, float g, uint8_t* packed8, uint8_t* scale1
 
 // Quantise n tokens token-major. kv_dtype FP8: out_data [n][576] E4M3 bytes (FP8 sources are
 // copied; BF16 sources go through c2). kv_dtype NVFP4: out_data [n][288] packed E2M1 pairs and
-// out_scale [n][36] E4M3 block scales (c3 per block of 16 consecutive channels).
+// out_scale [n][36] E4M3 block scales (c3 per block of 16 consecutive channels). kv_dtype FP8_PT:
+// out_data [n][576] E4M3 codes and out_scale [n] FP32 token scales as 4 little-endian bytes (c9).
 int qo_quant_tokens(const void* src, int src_dtype, int64_t n, int kv_dtype, float g,
                     uint8_t* out_data, uint8_t* out_scale, int threads) {
   if (src_dtype != SRC_FP8 && src_dtype != SRC_BF16) return -2;
-  if (kv_dtype != KV_FP8 && kv_dtype != KV_NVFP4) return -2;
+  if (kv_dtype != KV_FP8 && kv_dtype != KV_NVFP4 && kv_dtype != KV_FP8_PT) return -2;
   parallel_for(n, threads, [&](int64_t t) {
+    if (kv_dtype == KV_FP8_PT) {
+      float x[kLatent], sigma;
+      for (int i = 0; i < kLatent; ++i) x[i] = src_value(src, src_dtype, t, i);
+      pt_token(x, out_data + t * kLatent, &sigma);
+      std::memcpy(out_scale + 4 * t, &sigma, 4);
+      return;
+    }
     if (kv_dtype == KV_FP8) {
       for (int i = 0; i < kLatent; ++i) {
         out_data[t * kLatent + i] = (src_dtype == SRC_FP8)
@@ -243,11 +285,13 @@ int qo_quant_tokens(const void* src, int src_dtype, int64_t n, int kv_dtype, flo
 
 // The paged write of quantize-on-append: token n goes to slot slots[n] (page * page_size +
 // offset) of the pool; negative slots are skipped. Pools: FP8 [pages][page_size][576];
-// NVFP4 data [pages][page_size][288] and scales [pages][page_size][36].
+// NVFP4 data [pages][page_size][288] and scales [pages][page_size][36]; FP8_PT [pages][37,120]
+// (c9 layout, page_size 64).
 int qo_append(const void* src, int src_dtype, int64_t n, const int64_t* slots, int kv_dtype,
               float g, int page_size, int64_t num_pages, uint8_t* pool_data, uint8_t* pool_scale) {
   const int64_t nslots = num_pages * page_size;
-  const int row = (kv_dtype == KV_FP8) ? kLatent : kPackedPerToken;
+  if (kv_dtype == KV_FP8_PT && page_size != kPagePT) return -2;
+  const int row = (kv_dtype == KV_NVFP4) ? kPackedPerToken : kLatent;
   std::vector<uint8_t> d(row), s(kBlocksPerToken);
   for (int64_t t = 0; t < n; ++t) {
     const int64_t slot = slots[t];
@@ -258,6 +302,12 @@ int qo_append(const void* src, int src_dtype, int64_t n, const int64_t* slots, i
     else one = reinterpret_cast<const uint8_t*>(static_cast<const uint16_t*>(src) + t * kLatent);
     int rc = qo_quant_tokens(one, src_dtype, 1, kv_dtype, g, d.data(), s.data(), 1);
     if (rc) return rc;
+    if (kv_dtype == KV_FP8_PT) {
+      uint8_t* page = pool_data + (slot / kPagePT) * kPageBytesPT;
+      std::memcpy(page + (slot % kPagePT) * kLatent, d.data(), kLatent);
+      std::memcpy(page + kPagePT * kLatent + (slot % kPagePT) * 4, s.data(), 4);
+      continue;
+    }
     std::memcpy(pool_data + slot * row, d.data(), row);
     if (kv_dtype == KV_NVFP4) std::memcpy(pool_scale + slot * kBlocksPerToken, s.data(), kBlocksPerToken);
   }
@@ -268,8 +318,16 @@ int qo_append(const void* src, int src_dtype, int64_t n, const int64_t* slots, i
 //   FP8:   x_i = value(byte_i)
 //   NVFP4: x_i = g * value(s8_{i/16}) * value(c_i)
 //   BF16:  x_i = the BF16 value
+//   FP8_PT: x_i = sigma * value(c_i), slot = page * 64 + offset in the c9 page layout
 void qo_dequant_slot(const void* kv_data, const uint8_t* kv_scale, int kv_dtype, double g,
                      int64_t slot, double* x) {
+  if (kv_dtype == KV_FP8_PT) {
+    const uint8_t* page = static_cast<const uint8_t*>(kv_data) + (slot / kPagePT) * kPageBytesPT;
+    float sigma;
+    std::memcpy(&sigma, page + kPagePT * kLatent + (slot % kPagePT) * 4, 4);
+    for (int i = 0; i < kLatent; ++i) x[i] = static_cast<double>(sigma) * e4m3_value(page[(slot % kPagePT) * kLatent + i]);
+    return;
+  }
   for (int i = 0; i < kLatent; ++i) {
     if (kv_dtype == KV_FP8) {
       x[i] = e4m3_value(static_cast<const uint8_t*>(kv_data)[slot * kLatent + i]);
@@ -296,6 +354,7 @@ int qo_mla_decode(const uint16_t* q_bf16, int batch, int heads, const void* kv_d
                   double sm_scale, double g, const int32_t* pairs, int64_t npairs,
                   double* out_o, double* out_lse, int threads) {
   std::atomic<int> err{0};
+  if (kv_dtype == KV_FP8_PT && page_size != kPagePT) return -2;
   const int64_t n = pairs ? npairs : static_cast<int64_t>(batch) * heads;
   parallel_for(n, threads, [&](int64_t p) {
     const int r = pairs ? pairs[2 * p] : static_cast<int>(p / heads);
