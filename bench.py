@@ -172,6 +172,10 @@ class Problem:
         elif kv == q.KV_BF16:
             self.data = torch.empty((w.num_pages, 64, LATENT), dtype=torch.int16, device=dev)
             self.scale = None
+        elif kv == q.KV_FP8_PER_TOKEN:
+            self.data = torch.full((w.num_pages, q.PAGE_BYTES_FP8_PER_TOKEN), 0xFF, dtype=torch.uint8, device=dev)
+            self.scale = None
+            q.kv_append_quant(w.src_fp8, q.SRC_FP8_E4M3, w.slots, self.data, None, kv, 1.0)
         else:
             self.data, self.scale = w.pool_fp8, None
         self.lens = w.kv_len.copy()
@@ -187,7 +191,7 @@ class Problem:
         self.out = torch.empty((w.batch, w.heads, DV), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((w.batch, w.heads), dtype=torch.float32, device=dev)
         self.tokens = int(self.lens.sum())
-        bpt = {q.KV_FP8_E4M3: LATENT, q.KV_NVFP4: 324, q.KV_BF16: 2 * LATENT}[kv]
+        bpt = {q.KV_FP8_E4M3: LATENT, q.KV_NVFP4: 324, q.KV_BF16: 2 * LATENT, q.KV_FP8_PER_TOKEN: LATENT + 4}[kv]
         self.kv_bytes = self.tokens * bpt
         self.flops = self.tokens * w.heads * FLOPS_PER_TOKEN_HEAD
         self.needs_combine = self.plan.num_split_requests > 0 or self.plan.num_empty_requests > 0
@@ -479,6 +483,14 @@ def extra_workloads(q, pk, dev, args, main_w=None):
     # heads sweep of the headline shape (FP8 44 x 32K) at 16 / 32 / 64 heads
     if main_w is not None:
         res["heads_sweep_mla_fp8_b44_l32k"] = heads_sweep(q, pk, main_w, q.KV_FP8_E4M3, args, steps)
+        # the same tokens in the per-token-scaled FP8 layout (580 bytes per token)
+        pt = Problem(q, main_w, q.KV_FP8_PER_TOKEN, algo=args.algo)
+        ms, att = time_problem(pt, steps, args.warmup)
+        res["mla_fp8_per_token_b44_h128_l32k"] = summarize(pt, ms, att, pk)
+        del pt
+        res["heads_sweep_mla_fp8_per_token_b44_l32k"] = heads_sweep(q, pk, main_w, q.KV_FP8_PER_TOKEN, args, steps,
+                                                                   heads=(16,))
+        torch.cuda.empty_cache()
     # NVFP4, 10 x 163,840 (+1 appended per step), 128 heads
     w = synth.workload("mla_nvfp4_b10_h128_l160k", device=dev)
     pb = Problem(q, w, q.KV_NVFP4, g=1.0, append=True, algo=args.algo)

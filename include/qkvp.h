@@ -26,6 +26,13 @@
  *                of byte k, 2k+1 in the high nibble) and kv_scale uint8 [num_pages][64][36] E4M3
  *                block scales (block j covers elements 16j..16j+15). 324 bytes per token = 9/16 of
  *                FP8. An element decodes to global_scale * scale(block) * e2m1(code).
+ *  - FP8 pool with per-token scales (QKVP_KV_FP8_PER_TOKEN): kv_data uint8 [num_pages][37120]:
+ *                page p holds the 64 token rows of 576 E4M3 codes (bytes 0..36863), then the 64
+ *                FP32 token scales (bytes 36864..37119, little-endian). 580 bytes per token. An
+ *                element decodes to scale(token) * e4m3(code). The layout is the pages' indexer key
+ *                cache (FP8 elements + 4 scale bytes per token in a paged [npages, page_bytes] uint8
+ *                buffer, 64 tokens per page: "The Precision Frontier: Implementing bf16 Index Keys",
+ *                section "The Message: Planning the bf16-K Implementation") carrying the latent.
  *  - BF16 pool : kv_data uint16 [num_pages][64][576] (the cast-then-attend baseline only).
  *  - q         : bf16 [batch][num_heads][576], row-major, contiguous.
  *  - out       : bf16 [batch][num_heads][512], 16-byte aligned (the attend kernels store 16-byte
@@ -62,7 +69,12 @@ typedef enum {
   QKVP_E_CUDA = -4         /* a CUDA runtime call or launch failed */
 } qkvp_status;
 
-typedef enum { QKVP_KV_FP8_E4M3 = 1, QKVP_KV_NVFP4 = 2, QKVP_KV_BF16 = 3 } qkvp_kv_dtype;
+typedef enum {
+  QKVP_KV_FP8_E4M3 = 1,
+  QKVP_KV_NVFP4 = 2,
+  QKVP_KV_BF16 = 3,
+  QKVP_KV_FP8_PER_TOKEN = 4
+} qkvp_kv_dtype;
 typedef enum { QKVP_SRC_FP8_E4M3 = 1, QKVP_SRC_BF16 = 2 } qkvp_src_dtype;
 
 /* Decode kernel families. AUTO lets the planner choose. */
@@ -113,16 +125,20 @@ typedef struct {
  *               (QKVP_SRC_BF16).
  *  slot_mapping device int64 [n_tokens]: destination slot page * page_size + offset; a negative slot
  *               skips the token; a slot >= num_pages * page_size is skipped too.
- *  kv_data      device pool (layout above) for kv_dtype QKVP_KV_FP8_E4M3 or QKVP_KV_NVFP4.
- *  kv_scale     device NVFP4 block-scale pool; must be NULL for FP8.
+ *  kv_data      device pool (layout above) for kv_dtype QKVP_KV_FP8_E4M3, QKVP_KV_NVFP4 or
+ *               QKVP_KV_FP8_PER_TOKEN.
+ *  kv_scale     device NVFP4 block-scale pool; must be NULL for the FP8 pools.
  *  global_scale NVFP4 decode multiplier g (> 0, finite): an element decodes to g * s * e. Must be
- *               1.0 for FP8.
+ *               1.0 for the FP8 pools.
  *
  * FP8 pool: FP8 sources are copied; BF16 sources round to nearest even, saturating at +-448; NaN
  * gives 0x7F. NVFP4 pool, per block of 16 consecutive elements x (FP32 arithmetic, one rounding per
  * operation): amax = max|x| (NaN if any x is NaN); s8 = E4M3(amax / (6 g)) rounded to nearest even
  * and saturated; sd = value(s8) * g; codes = 0 where sd == 0, else E2M1(x / sd) rounded to nearest
- * even and saturated at +-6 (NaN gives 0). The stored bytes are bit-identical to the CPU oracle.
+ * even and saturated at +-6 (NaN gives 0). FP8 pool with per-token scales, per token x (FP32
+ * arithmetic, one rounding per operation): amax = max|x|; scale = amax / 448, or the NaN 0x7FC00000
+ * if any x is NaN; codes = E4M3(x / scale) rounded to nearest even and saturated (NaN gives 0x7F),
+ * or E4M3(x) (a signed zero) when scale == 0. The stored bytes are bit-identical to the CPU oracle.
  * If two tokens of one call name the same slot, which of them is stored is unspecified.
  */
 int kv_append_quant(const void* src, int32_t src_dtype, int64_t n_tokens,
@@ -261,7 +277,8 @@ int kv_pool_cast_bf16(const uint8_t* in, int64_t n_elems, void* out, qkvp_stream
  *  out                device uint8 [total_tokens][576], 16-byte aligned; every row is written.
  * Every table entry is bounds-checked on the device: a row whose entry lies outside the request's
  * pages, the table (nnz) or the pool (num_pages) is written as zeros. Errors: QKVP_E_INVALID for
- * bad arguments, QKVP_E_UNSUPPORTED for page_size != 64 or a BF16 pool.
+ * bad arguments, QKVP_E_UNSUPPORTED for page_size != 64, a BF16 pool or a per-token-scaled pool
+ * (whose scale has no place in a plain E4M3 workspace).
  */
 int kv_gather_fp8(const void* kv_data, const uint8_t* kv_scale, int32_t kv_dtype, float global_scale,
                   int32_t page_size, int64_t num_pages, const int32_t* kv_indptr, const int32_t* kv_indices,

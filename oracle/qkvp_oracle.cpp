@@ -160,9 +160,11 @@ void nvfp4_block(const float* x, float g, uint8_t* packed, uint8_t* scale) {
 // 576 + 4 bytes per token. The pages give no formula for the scale; the one here maps the token's
 // largest magnitude onto E4M3's largest finite value (448, c1). FP32 throughout, one rounding per
 // operation:
-//   amax  = max |x_i|                     (NaN if any x_i is NaN)
-//   sigma = amax / 448
-//   c_i   = E4M3(x_i / sigma)             (c2), or E4M3(x_i) (a signed zero) when sigma == 0
+//   amax  = max |x_i|
+//   sigma = amax / 448, or the NaN 0x7FC00000 if any x_i is NaN (one fixed pattern for the stored
+//           bytes: a division's NaN result carries no portable payload)
+//   c_i   = E4M3(x_i / sigma)             (c2; 0x7F for every element of a NaN token), or
+//           E4M3(x_i) (a signed zero) when sigma == 0
 // The value of element i is sigma * value(c_i).
 void pt_token(const float* x, uint8_t* codes, float* sigma) {
   float amax = 0.0f;
@@ -172,8 +174,11 @@ void pt_token(const float* x, uint8_t* codes, float* sigma) {
     const float a = std::fabs(x[i]);
     if (a > amax) amax = a;
   }
-  if (nan) amax = NAN;
-  const float s = amax / 448.0f;
+  float s = amax / 448.0f;
+  if (nan) {
+    const uint32_t qnan = 0x7FC00000u;
+    std::memcpy(&s, &qnan, 4);
+  }
   for (int i = 0; i < kLatent; ++i) codes[i] = (s == 0.0f) ? e4m3_encode(x[i]) : e4m3_encode(x[i] / s);
   *sigma = s;
 }

@@ -6,9 +6,15 @@
 // pages give no arithmetic for the block scale; the one used here, and by the CPU oracle, is:
 // amax / (6 g) rounded to nearest-even E4M3, element codes E2M1(x / (scale * g)).
 //
+// The per-token-scaled FP8 pool carries the pages' indexer key layout ("The Precision Frontier:
+// Implementing bf16 Index Keys", section "The Message: Planning the bf16-K Implementation": FP8
+// elements + 4 scale bytes per token, 64-token pages) for the latent: one FP32 scale per token,
+// amax / 448, and codes E4M3(x / scale).
+//
 // One thread quantises one block of 16 consecutive latent elements of one token (36 blocks per
-// token); the append of a decode step touches a handful of tokens, a bulk fill touches millions,
-// and both are bound by reading the source.
+// token; one warp per token for the per-token-scaled pool, whose scale needs the whole token); the
+// append of a decode step touches a handful of tokens, a bulk fill touches millions, and both are
+// bound by reading the source.
 #include <cstdint>
 
 #include "qkvp_device.cuh"
@@ -98,6 +104,48 @@ __global__ void append_nvfp4_kernel(const void* __restrict__ src, int src_dtype,
   scale[slot * kScales + blk] = static_cast<uint8_t>(s8);
 }
 
+__global__ void append_fp8pt_kernel(const void* __restrict__ src, int src_dtype, int64_t n,
+                                    const int64_t* __restrict__ slots, uint8_t* __restrict__ pool,
+                                    int64_t num_slots) {
+  const int64_t tok = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (tok >= n) return;                       // tok and slot are the same for the whole warp
+  const int64_t slot = slots[tok];
+  if (slot < 0 || slot >= num_slots) return;
+  constexpr int kExtra = kBlocks - 32;        // lanes 0..3 hold a second block (blocks 32..35)
+  float x0[16], x1[16];
+  load16(src, src_dtype, tok, lane, x0);
+  if (lane < kExtra) load16(src, src_dtype, tok, 32 + lane, x1);
+  float amax = 0.0f;
+  bool nan = false;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    nan |= (x0[i] != x0[i]);
+    amax = fmaxf(amax, fabsf(x0[i]));
+    if (lane < kExtra) {
+      nan |= (x1[i] != x1[i]);
+      amax = fmaxf(amax, fabsf(x1[i]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  // a token holding a NaN gets the scale 0x7FC00000 (one fixed NaN pattern for the stored bytes)
+  const bool any_nan = __any_sync(0xffffffffu, nan);
+  const float sc = any_nan ? __uint_as_float(0x7FC00000u) : __fdiv_rn(amax, 448.0f);
+  uint8_t* page = pool + (slot / kPage) * kPtPageBytes;
+  uint8_t* row = page + (slot % kPage) * kLatent;
+  auto encode16 = [&](const float (&x)[16], int blk) {
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[i / 4] |= dev::encode_e4m3(sc == 0.0f ? x[i] : __fdiv_rn(x[i], sc)) << (8 * (i % 4));
+    *reinterpret_cast<uint4*>(row + blk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  };
+  encode16(x0, lane);
+  if (lane < kExtra) encode16(x1, 32 + lane);
+  if (lane == 0) *reinterpret_cast<float*>(page + kPtScaleOff + (slot % kPage) * 4) = sc;
+}
+
 __global__ void encode_kernel(const float* __restrict__ x, int64_t n, int fmt, uint8_t* __restrict__ out) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -140,6 +188,9 @@ cudaError_t launch_append(const void* src, int src_dtype, int64_t n, const int64
   const int64_t blocks = (n * kBlocks + threads - 1) / threads;
   if (kv_dtype == KV_FP8) {
     append_fp8_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+        src, src_dtype, n, slots, static_cast<uint8_t*>(kv_data), num_slots);
+  } else if (kv_dtype == KV_FP8PT) {
+    append_fp8pt_kernel<<<static_cast<unsigned>((n + threads / 32 - 1) / (threads / 32)), threads, 0, s>>>(
         src, src_dtype, n, slots, static_cast<uint8_t*>(kv_data), num_slots);
   } else {
     append_nvfp4_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(

@@ -124,9 +124,10 @@ int kv_append_quant(const void* src, int32_t src_dtype, int64_t n_tokens, const 
                     int32_t page_size, int64_t num_pages, qkvp_stream_t stream) {
   if (n_tokens < 0 || num_pages < 0) return QKVP_E_INVALID;
   if (src_dtype != QKVP_SRC_FP8_E4M3 && src_dtype != QKVP_SRC_BF16) return QKVP_E_UNSUPPORTED;
-  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4) return QKVP_E_UNSUPPORTED;
+  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_FP8_PER_TOKEN)
+    return QKVP_E_UNSUPPORTED;
   if (page_size != QKVP_PAGE_SIZE) return QKVP_E_UNSUPPORTED;
-  if (kv_dtype == QKVP_KV_FP8_E4M3) {
+  if (kv_dtype != QKVP_KV_NVFP4) {
     if (kv_scale != nullptr || global_scale != 1.0f) return QKVP_E_INVALID;
   } else {
     if (kv_scale == nullptr || !finite_float(global_scale) || !(global_scale > 0.0f)) return QKVP_E_INVALID;
@@ -151,7 +152,8 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   if (batch > 0 && (!kv_indptr_host || !kv_len_host)) return QKVP_E_INVALID;
   if (page_size != QKVP_PAGE_SIZE) return QKVP_E_UNSUPPORTED;
   if (num_heads < 16 || num_heads > 128 || num_heads % 16) return QKVP_E_UNSUPPORTED;
-  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16)
+  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16 &&
+      kv_dtype != QKVP_KV_FP8_PER_TOKEN)
     return QKVP_E_UNSUPPORTED;
   // the tcgen05 CTA-pair kernel needs exactly 128 heads; other head counts use the mma.sync kernel
   if (algo == QKVP_ALGO_AUTO) algo = num_heads == 128 ? QKVP_ALGO_TCGEN05 : QKVP_ALGO_MMA_SYNC;
@@ -316,7 +318,7 @@ int kv_gather_fp8(const void* kv_data, const uint8_t* kv_scale, int32_t kv_dtype
                   int64_t nnz, const int64_t* tok_indptr, int32_t batch, int64_t total_tokens, uint8_t* out,
                   qkvp_stream_t stream) {
   if (page_size != kPage) return QKVP_E_UNSUPPORTED;
-  if (kv_dtype == QKVP_KV_BF16) return QKVP_E_UNSUPPORTED;
+  if (kv_dtype == QKVP_KV_BF16 || kv_dtype == QKVP_KV_FP8_PER_TOKEN) return QKVP_E_UNSUPPORTED;
   if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4) return QKVP_E_INVALID;
   if (batch < 0 || total_tokens < 0 || nnz < 0 || num_pages < 0) return QKVP_E_INVALID;
   if (kv_dtype == QKVP_KV_NVFP4) {

@@ -35,10 +35,12 @@ namespace {
 
 constexpr int kRow = kLatent + 8;          // padded smem row of the 16-bit tiles (1168 bytes)
 constexpr int kRowBytes = kRow * 2;
+constexpr int kSigByte = kLatent * 2;      // a per-token-scaled page keeps the token's scale here
 
 template <int KV>
 constexpr int raw_bytes() {
-  return KV == KV_FP8 ? kPage * kLatent : (KV == KV_NVFP4 ? kPage * (kPacked + kScales) : 0);
+  return KV == KV_FP8 ? kPage * kLatent
+       : KV == KV_NVFP4 ? kPage * (kPacked + kScales) : KV == KV_FP8PT ? kPtPageBytes : 0;
 }
 
 constexpr int kNT = 256;                   // threads per CTA: every warp dequantizes
@@ -58,7 +60,8 @@ constexpr int smem_bytes() {
   return HC * kRowBytes + kPage * kRowBytes + raw_bufs<KV, HC>() * raw_bytes<KV>() + pairs<HC>() * 2 * 32 * 32 * 4 + 64;
 }
 
-// Raw bytes of one page (FP8: the page; NVFP4: data then block scales) into a raw buffer with bulk
+// Raw bytes of one page (FP8, per-token-scaled FP8: the page; NVFP4: data then block scales) into a
+// raw buffer with bulk
 // asynchronous copies, counted on `bar` (one expect-tx arrival by the issuing thread). A page id
 // outside the pool copies nothing; the arrival alone completes the phase and the page reads as empty.
 template <int KV>
@@ -67,9 +70,9 @@ __device__ __forceinline__ void fetch_page(const DecodeArgs& a, int64_t page, ui
     tc::mbar_arrive(bar);
     return;
   }
-  if (KV == KV_FP8) {
-    tc::mbar_arrive_expect_tx(bar, kPage * kLatent);
-    tc::bulk_load(s_raw, a.kv + page * (kPage * kLatent), kPage * kLatent, bar);
+  if (KV == KV_FP8 || KV == KV_FP8PT) {
+    tc::mbar_arrive_expect_tx(bar, raw_bytes<KV>());
+    tc::bulk_load(s_raw, a.kv + page * raw_bytes<KV>(), raw_bytes<KV>(), bar);
   } else {
     tc::mbar_arrive_expect_tx(bar, kPage * (kPacked + kScales));
     tc::bulk_load(s_raw, a.kv + page * (kPage * kPacked), kPage * kPacked, bar);
@@ -119,6 +122,26 @@ __device__ __forceinline__ void dequant_page(const uint8_t* s_raw, uint8_t* s_kv
       dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
       dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
+  } else if (KV == KV_FP8PT) {
+    // the codes exactly (as FP8), the token scale into the row's padding: it multiplies the token's
+    // logit and its probability in FP32, so no operand carries an extra rounding
+    for (int c = tid; c < valid * (kLatent / 16); c += NT) {
+      const int row = c / (kLatent / 16), ch = c % (kLatent / 16);
+      const uint4 v = *reinterpret_cast<const uint4*>(s_raw + c * 16);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        o[2 * k] = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+        o[2 * k + 1] = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(w[k] >> 16));
+      }
+      uint4* dst = reinterpret_cast<uint4*>(s_kv + row * kRowBytes + ch * 32);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    const float* s_sc = reinterpret_cast<const float*>(s_raw + kPtScaleOff);
+    for (int row = tid; row < kPage; row += NT)
+      *reinterpret_cast<float*>(s_kv + row * kRowBytes + kSigByte) = row < valid ? s_sc[row] : 0.0f;
   } else if (KV == KV_NVFP4) {
     const uint8_t* s_sc = s_raw + kPage * kPacked;
     for (int c = tid; c < valid * (kPacked / 16); c += NT) {
@@ -314,13 +337,22 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
           s[n][i] = half == 0 ? (s[n][i] + peer) : (peer + s[n][i]);
         }
       // ---- online softmax in base 2 (rows g8 and g8 + 8 of the 16 heads) ----
+      // per-token-scaled pages: the token scale multiplies the logit and the probability (not l)
+      float sig[2 * NP][2];
+#pragma unroll
+      for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          sig[n][e] = KV == KV_FP8PT
+              ? *reinterpret_cast<const float*>(s_kv + (t0 + n * 8 + 2 * t4 + e) * kRowBytes + kSigByte) : 1.0f;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tok = t0 + n * 8 + 2 * t4 + (i & 1);
-          const float v = tok < live ? s[n][i] * q_scale_log2 : -INFINITY;
+          const float x = KV == KV_FP8PT ? s[n][i] * sig[n][i & 1] : s[n][i];
+          const float v = tok < live ? x * q_scale_log2 : -INFINITY;
           s[n][i] = v;
           mx[i >> 1] = fmaxf(mx[i >> 1], v);
         }
@@ -351,10 +383,12 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
       // ---- O[:, my 256 dims] += P V ----
 #pragma unroll
       for (int kt = 0; kt < NP; ++kt) {
-        const uint32_t pa0 = dev::pack_f16x2(s[2 * kt][0], s[2 * kt][1]);
-        const uint32_t pa1 = dev::pack_f16x2(s[2 * kt][2], s[2 * kt][3]);
-        const uint32_t pa2 = dev::pack_f16x2(s[2 * kt + 1][0], s[2 * kt + 1][1]);
-        const uint32_t pa3 = dev::pack_f16x2(s[2 * kt + 1][2], s[2 * kt + 1][3]);
+        const float* sa = sig[2 * kt];
+        const float* sb = sig[2 * kt + 1];
+        const uint32_t pa0 = dev::pack_f16x2(s[2 * kt][0] * sa[0], s[2 * kt][1] * sa[1]);
+        const uint32_t pa1 = dev::pack_f16x2(s[2 * kt][2] * sa[0], s[2 * kt][3] * sa[1]);
+        const uint32_t pa2 = dev::pack_f16x2(s[2 * kt + 1][0] * sb[0], s[2 * kt + 1][1] * sb[1]);
+        const uint32_t pa3 = dev::pack_f16x2(s[2 * kt + 1][2] * sb[0], s[2 * kt + 1][3] * sb[1]);
 #pragma unroll
         for (int vp = 0; vp < 16; ++vp) {
           uint32_t b0, b1, b2, b3;
@@ -481,6 +515,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s) {
     case KV_FP8: return launch_kv<KV_FP8>(a, s);
     case KV_NVFP4: return launch_kv<KV_NVFP4>(a, s);
     case KV_BF16: return launch_kv<KV_BF16>(a, s);
+    case KV_FP8PT: return launch_kv<KV_FP8PT>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -77,7 +77,8 @@ constexpr uint32_t OFF_P = OFF_V + kVSlots * kVSlot;
 constexpr uint32_t OFF_Q = OFF_P + 2 * kPBytes;
 constexpr uint32_t OFF_RM = OFF_Q + kQSmemAtoms * kQAtom;   // 2 x 128 FP32: the peer's row maxima
 constexpr uint32_t OFF_LX = OFF_RM + 2 * 512;               // 2 x 128 FP32: the peer's row sums
-constexpr uint32_t OFF_BAR = OFF_LX + 2 * 512;
+constexpr uint32_t OFF_SIG = OFF_LX + 2 * 512;             // per V slot, the own 32 tokens' scales
+constexpr uint32_t OFF_BAR = OFF_SIG + kVSlots * 128;
 enum : uint32_t {
   B_K_FULL = 0, B_K_EMPTY = 2, B_V_FULL = 4, B_V_EMPTY = 7, B_S_FULL = 10, B_S_FREE = 12, B_P_LOCAL = 14,
   B_P_FULL = 16, B_P_FREE = 18, B_O_DONE = 20, B_Q_READY = 22, B_FINAL = 23, B_RM_FULL = 24, B_LX_FULL = 26,
@@ -184,7 +185,8 @@ template <> struct Dequant<KV_FP8> {
       if (q < kItems && it.tok < valid) ldg_nc32(base + it.tok * kLatent + it.dim, r.v[i]);
     }
   }
-  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int c, int t, uint32_t ks, uint32_t vs) {
+  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int c, int t, uint32_t ks, uint32_t vs,
+                               uint32_t) {
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
       const int q = t + kDQ * i;
@@ -198,6 +200,40 @@ template <> struct Dequant<KV_FP8> {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         sts128(at + tc::sw128_offset(it.row, ch + u), make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
+    }
+  }
+};
+
+template <> struct Dequant<KV_FP8PT> {
+  // the FP8 items (codes converted exactly); the own tokens' scales go to the V slot's scale array,
+  // zero past the valid tokens, for the softmax to apply in FP32
+  static constexpr int kOwn = Dequant<KV_FP8>::kOwn, kItems = Dequant<KV_FP8>::kItems;
+  static constexpr int kIters = Dequant<KV_FP8>::kIters;
+  struct Raw { Dequant<KV_FP8>::Raw codes; float s[kIters]; };
+  __device__ static Item at(int q, int c) { return Dequant<KV_FP8>::at(q, c); }
+  __device__ static void load(Raw& r, const DecodeArgs& a, int64_t page, int valid, int c, int t) {
+    const uint8_t* base = a.kv + page * kPtPageBytes;
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      const int q = t + kDQ * i;
+      const Item it = at(q, c);
+      if (q < kItems && it.tok < valid) {
+        ldg_nc32(base + it.tok * kLatent + it.dim, r.codes.v[i]);
+        // one scale per own token: loaded by the item that stores it (the per-SM queue of
+        // outstanding loads, not bandwidth, limits this loop)
+        if (q < kOwn && it.dim == 0) r.s[i] = __ldg(reinterpret_cast<const float*>(base + kPtScaleOff) + it.tok);
+      }
+    }
+  }
+  __device__ static void store(const Raw& r, const DecodeArgs& a, int64_t page, int valid, int c, int t, uint32_t ks,
+                               uint32_t vs, uint32_t sg) {
+    Dequant<KV_FP8>::store(r.codes, a, page, valid, c, t, ks, vs, sg);
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      const int q = t + kDQ * i;
+      if (q >= kOwn) continue;
+      const Item it = at(q, c);
+      if (it.dim == 0) tc::sts_f32(sg + 4 * it.row, it.tok < valid ? r.s[i] : 0.0f);
     }
   }
 };
@@ -224,7 +260,8 @@ template <> struct Dequant<KV_NVFP4> {
       }
     }
   }
-  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int c, int t, uint32_t ks, uint32_t vs) {
+  __device__ static void store(const Raw& r, const DecodeArgs&, int64_t, int valid, int c, int t, uint32_t ks, uint32_t vs,
+                               uint32_t) {
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
       const int q = t + kDQ * i;
@@ -260,7 +297,8 @@ template <> struct Dequant<KV_BF16> {      // the cast-then-attend baseline: BF1
     return item_at(kOwn, q, c, 256, 8 * (qq & 7), (qq >> 3) & 31);
   }
   __device__ static void load(Raw&, const DecodeArgs&, int64_t, int, int, int) {}
-  __device__ static void store(const Raw&, const DecodeArgs& a, int64_t page, int valid, int c, int t, uint32_t ks, uint32_t vs) {
+  __device__ static void store(const Raw&, const DecodeArgs& a, int64_t page, int valid, int c, int t, uint32_t ks, uint32_t vs,
+                               uint32_t) {
     const uint8_t* base = a.kv + page * (kPage * kLatent * 2);
 #pragma unroll 1
     for (int r0 = 0; r0 < kItems; r0 += kDQ * kRound) {
@@ -331,7 +369,7 @@ __device__ bool wait_counter(const Sync& sy, uint32_t addr, uint32_t target) {
 // ---- roles -------------------------------------------------------------------------------------------
 template <int KV>
 __device__ void role_dequant(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, int t, uint32_t kring,
-                             uint32_t vring) {
+                             uint32_t vring, uint32_t sigring) {
   using D = Dequant<KV>;
   // Page indices are read one page before they are needed (raw loads of page g + 1 are issued while
   // page g is converted, with the index of page g + 2 already in flight), so no iteration waits on a
@@ -357,7 +395,7 @@ __device__ void role_dequant(const DecodeArgs& a, const Sync& sy, int seg_b, int
     // phase), the V slot by page g - 3 (its P.V completion)
     if (g >= kKSlots && !sy.wait(B_K_EMPTY + kb, ((g / kKSlots) - 1) & 1, false, 2)) return;
     if (g >= kVSlots && !sy.wait(B_V_EMPTY + vb, ((g / kVSlots) - 1) & 1, false, 2)) return;
-    D::store(raw_cur, a, pg, valid, c, t, kring + kb * kKSlot, vring + vb * kVSlot);
+    D::store(raw_cur, a, pg, valid, c, t, kring + kb * kKSlot, vring + vb * kVSlot, sigring + vb * 128);
     tc::fence_proxy_async_smem();
     // the V slot first: the Q.K^T threads wait only on the K slot and take it as "page written"
     tc::mbar_arrive(sy.bar(B_V_FULL + vb));
@@ -471,7 +509,8 @@ __device__ void role_pv(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_
 // CTA's row maxima of page g + 1, which this CTA sends after it has read the slot of page g.
 template <int KV>
 __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, int h,
-                             uint32_t tbase, uint32_t pbuf, uint32_t qs, uint32_t rm, uint32_t lx, uint32_t qver) {
+                             uint32_t tbase, uint32_t pbuf, uint32_t qs, uint32_t rm, uint32_t lx, uint32_t qver,
+                             const float* sig) {
   const uint32_t peer = c ^ 1u;
   const uint32_t tl = tbase + (static_cast<uint32_t>(h & ~31) << 16);   // this warp's TMEM lane quarter
   auto wait = [&](uint32_t bar, uint32_t parity, bool cluster, int code) -> bool {
@@ -552,6 +591,11 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
 
     // ---- logits of the own tokens (buffer s; refilled for page g + 2 only after S_FREE(s)) ----
     if (!wait(B_S_FULL + s, (g >> 1) & 1, false, 128)) return;
+    // per-token-scaled pages: the own tokens' scales sit beside V slot g % 3 (written with it; the
+    // slot is refilled only after this page's P.V, which needs this thread's P first). Each scale
+    // multiplies its token's logit and probability in FP32 (not the row sum).
+    const float* sgp = sig + (g % kVSlots) * 32;
+    if (KV == KV_FP8PT && !wait(B_V_FULL + g % kVSlots, (g / kVSlots) & 1, false, 128)) return;
     tc::tc_fence_after();
     uint32_t sr[32];
     tc::tmem_ld32(tl + TM_S + kHalf * s, sr);
@@ -561,6 +605,16 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
     float x[32], mx8[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+    if (KV == KV_FP8PT) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 sg4 = reinterpret_cast<const float4*>(sgp)[u];
+        sr[4 * u] = __float_as_uint(__uint_as_float(sr[4 * u]) * sg4.x);
+        sr[4 * u + 1] = __float_as_uint(__uint_as_float(sr[4 * u + 1]) * sg4.y);
+        sr[4 * u + 2] = __float_as_uint(__uint_as_float(sr[4 * u + 2]) * sg4.z);
+        sr[4 * u + 3] = __float_as_uint(__uint_as_float(sr[4 * u + 3]) * sg4.w);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       x[i] = i < nv ? __uint_as_float(sr[i]) : -INFINITY;
@@ -587,7 +641,12 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
         const float p0 = dev::fast_exp2(fmaf(x[2 * i], q_scale, -mref));
         const float p1 = dev::fast_exp2(fmaf(x[2 * i + 1], q_scale, -mref));
         l4[i & 3] += p0 + p1;
-        pk[i] = dev::pack_f16x2(p0, p1);
+        if (KV == KV_FP8PT) {
+          const float2 sg2 = reinterpret_cast<const float2*>(sgp)[i];
+          pk[i] = dev::pack_f16x2(p0 * sg2.x, p1 * sg2.y);
+        } else {
+          pk[i] = dev::pack_f16x2(p0, p1);
+        }
       }
       lsum = (l4[0] + l4[1]) + (l4[2] + l4[3]);
     };
@@ -740,9 +799,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 
   if (warp < 4) {
     role_softmax<KV>(a, sy, seg_b, seg_e, c, tid, tbase, base + OFF_P, base + OFF_Q, base + OFF_RM, base + OFF_LX,
-                     base + OFF_QVER);
+                     base + OFF_QVER, reinterpret_cast<const float*>(sbase + OFF_SIG));
   } else if (warp < kQkWarpOdd) {
-    role_dequant<KV>(a, sy, seg_b, seg_e, c, tid - 128, base + OFF_K, base + OFF_V);
+    role_dequant<KV>(a, sy, seg_b, seg_e, c, tid - 128, base + OFF_K, base + OFF_V, base + OFF_SIG);
   } else if (warp == kPvWarp) {
     if ((tid & 31) == 0) role_pv(a, sy, seg_b, seg_e, c, tbase, base + OFF_V, base + OFF_P);
   } else if ((tid & 31) == 0) {
@@ -810,6 +869,7 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
     case KV_FP8: return launch_kv<KV_FP8>(a, s);
     case KV_NVFP4: return launch_kv<KV_NVFP4>(a, s);
     case KV_BF16: return launch_kv<KV_BF16>(a, s);
+    case KV_FP8PT: return launch_kv<KV_FP8PT>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -113,7 +113,8 @@ extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* 
   if (batch < 0 || min_splits < 0) return QKVP_E_INVALID;
   if (batch > 0 && (!kv_indptr_host || !kv_len_host)) return QKVP_E_INVALID;
   if (num_heads < 16 || num_heads > 128 || num_heads % 16) return QKVP_E_UNSUPPORTED;
-  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16)
+  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16 &&
+      kv_dtype != QKVP_KV_FP8_PER_TOKEN)
     return QKVP_E_UNSUPPORTED;
   if (batch > kMaxBatch) return QKVP_E_WORKSPACE;
   if (batch > 0 && kv_indptr_host[0] != 0) return QKVP_E_INVALID;

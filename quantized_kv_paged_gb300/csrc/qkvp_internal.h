@@ -15,7 +15,10 @@ constexpr int kPacked = kLatent / 2;    // NVFP4 data bytes per token (two E2M1 
 constexpr int kScales = kLatent / 16;   // NVFP4 E4M3 block scales per token
 constexpr uint64_t kPlanMagic = 0x716b76702d706c31ull;
 
-enum : int { KV_FP8 = 1, KV_NVFP4 = 2, KV_BF16 = 3 };
+enum : int { KV_FP8 = 1, KV_NVFP4 = 2, KV_BF16 = 3, KV_FP8PT = 4 };
+// Per-token-scaled FP8 page: 64 rows of 576 E4M3 codes, then 64 FP32 token scales.
+constexpr int kPtScaleOff = kPage * kLatent;              // 36,864
+constexpr int kPtPageBytes = kPage * (kLatent + 4);       // 37,120
 enum : int { SRC_FP8 = 1, SRC_BF16 = 2 };
 enum : int { ALGO_AUTO = 0, ALGO_MMA = 1, ALGO_TC = 2 };
 

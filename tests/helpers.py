@@ -9,7 +9,7 @@ import oracle
 import quantized_kv_paged_gb300 as q
 import synth
 
-KV_NAMES = {q.KV_FP8_E4M3: "fp8", q.KV_NVFP4: "nvfp4", q.KV_BF16: "bf16"}
+KV_NAMES = {q.KV_FP8_E4M3: "fp8", q.KV_NVFP4: "nvfp4", q.KV_BF16: "bf16", q.KV_FP8_PER_TOKEN: "fp8_per_token"}
 
 # Tolerance on BF16 outputs, from the stated target: max-abs 2e-2, mean-abs 2e-3. It is applied to
 # the excess of |out - o_ref| over half a BF16 ulp of o_ref (the rounding any BF16 output carries);
@@ -28,6 +28,11 @@ def gpu_pools(w: synth.Workload, kv: int, g: float = 1.0):
         scale = torch.full((w.num_pages, 64, 36), 0x7F, dtype=torch.uint8, device=dev)
         q.kv_append_quant(w.src_fp8, q.SRC_FP8_E4M3, w.slots, data, scale, q.KV_NVFP4, g)
         return data, scale
+    if kv == q.KV_FP8_PER_TOKEN:
+        # slots never appended hold NaN codes and NaN scales: decode must never read them
+        data = torch.full((w.num_pages, q.PAGE_BYTES_FP8_PER_TOKEN), 0xFF, dtype=torch.uint8, device=dev)
+        q.kv_append_quant(w.src_fp8, q.SRC_FP8_E4M3, w.slots, data, None, q.KV_FP8_PER_TOKEN, 1.0)
+        return data, None
     out = torch.empty((w.num_pages, 64, 576), dtype=torch.int16, device=dev)
     q.kv_pool_cast_bf16(w.pool_fp8, out)
     return out, None
@@ -46,6 +51,15 @@ def oracle_pools(w: synth.Workload, kv: int, g: float = 1.0):
         data[slots] = d
         scale[slots] = s
         return data.reshape(w.num_pages, 64, 288), scale.reshape(w.num_pages, 64, 36)
+    if kv == q.KV_FP8_PER_TOKEN:
+        # the oracle's quantisation (threaded), placed at the slots by the c9 page layout
+        data = np.full((w.num_pages, oracle.PAGE_BYTES_PT), 0xFF, np.uint8)
+        codes, sig = oracle.quant_tokens(w.src_fp8.cpu().numpy(), oracle.SRC_FP8, oracle.KV_FP8_PT)
+        slots = w.slots.cpu().numpy()
+        page, off = slots // 64, slots % 64
+        data[:, :64 * 576].reshape(w.num_pages, 64, 576)[page, off] = codes
+        data[:, 64 * 576:].view(np.float32).reshape(w.num_pages, 64)[page, off] = sig
+        return data, None
     return oracle.cast_fp8_to_bf16(pool), None
 
 

@@ -51,6 +51,7 @@ def test_plan_rejects_bad_arguments(lib):
     for h in (8, 24 + 1, 144, 0):
         assert plan(ok_ptr, ok_len, heads=h).status == q.QKVP_E_UNSUPPORTED
     assert plan(ok_ptr, ok_len, kv=9).status == q.QKVP_E_UNSUPPORTED
+    assert plan(ok_ptr, ok_len, kv=q.KV_FP8_PER_TOKEN).status == q.QKVP_OK
     assert plan(np.array([1, 3], np.int32), ok_len).status == q.QKVP_E_INVALID       # indptr[0] != 0
     assert plan(np.array([0, 1], np.int32), ok_len).status == q.QKVP_E_INVALID       # 100 tokens, 1 page
     assert plan(np.array([0, 2], np.int32), np.array([-1], np.int32)).status == q.QKVP_E_INVALID
@@ -110,6 +111,9 @@ def test_run_and_append_reject_before_launch(lib):
     assert f(16, 1, 4, 16, 16, 16, 2, 0.0, 64, 10, None) == q.QKVP_E_INVALID      # g = 0
     assert f(16, 1, 4, 16, 16, 16, 2, float("nan"), 64, 10, None) == q.QKVP_E_INVALID
     assert f(16, 1, 4, 16, 16, 16, 3, 1.0, 64, 10, None) == q.QKVP_E_UNSUPPORTED  # BF16 pool
+    assert f(16, 1, 4, 16, 16, 16, 4, 1.0, 64, 10, None) == q.QKVP_E_INVALID      # per-token FP8 + scale pool
+    assert f(16, 1, 4, 16, 16, None, 4, 0.5, 64, 10, None) == q.QKVP_E_INVALID    # per-token FP8, g != 1
+    assert f(16, 1, 0, 16, 16, None, 4, 1.0, 64, 10, None) == q.QKVP_OK            # accepted, nothing to do
     assert f(16, 1, 4, 16, 16, 16, 2, 1.0, 32, 10, None) == q.QKVP_E_UNSUPPORTED  # page size
     assert f(None, 1, 4, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID
     assert f(17, 1, 4, 16, 16, 16, 2, 1.0, 64, 10, None) == q.QKVP_E_INVALID      # misaligned source
@@ -140,6 +144,7 @@ def test_gather_entry_points_reject_before_launch(lib):
                  a["b"], a["t"], a["out"], None)
     assert call(ps=32) == q.QKVP_E_UNSUPPORTED
     assert call(dt=3) == q.QKVP_E_UNSUPPORTED                 # BF16 pool
+    assert call(dt=4, sc=None) == q.QKVP_E_UNSUPPORTED        # per-token-scaled FP8 pool
     assert call(dt=7) == q.QKVP_E_INVALID
     assert call(g=0.0) == q.QKVP_E_INVALID
     assert call(g=float("inf")) == q.QKVP_E_INVALID

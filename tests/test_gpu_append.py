@@ -94,6 +94,44 @@ def test_append_fp8_bit_exact(qkvp, src_kind):
     assert np.array_equal(pool.cpu().numpy().reshape(-1, 576), hp)
 
 
+@pytest.mark.parametrize("src_kind", ["fp8", "bf16"])
+def test_append_fp8_per_token_bit_exact(qkvp, src_kind):
+    rng = np.random.default_rng(13)
+    n = 3000
+    x = (rng.standard_normal((n, 576)) * np.exp(rng.uniform(-30, 25, (n, 1)))).astype(np.float32)
+    x[::5, 100] *= 20
+    sp = _special_values()
+    if src_kind == "fp8":
+        src = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8)
+        src[3, 17] = 0x7F        # NaN byte: the token's scale is NaN, every code 0x7F
+        src[4] = 0               # all-zero token: scale 0, codes 0
+        src[5, 9] = 0x80         # -0 in an otherwise zero token
+        src[5, :9] = 0
+        src[5, 10:] = 0
+        src[6] = 0x01            # the smallest subnormal everywhere
+        src_np, sdt, sd = src.numpy(), oracle.SRC_FP8, q.SRC_FP8_E4M3
+    else:
+        x[0, :sp.size] = sp      # NaN token
+        x[1, :sp.size - 1] = np.delete(sp, np.nonzero(np.isnan(sp))[0][0])   # +-inf: the scale is inf
+        x[2] = 0.0
+        x[3] = 1e-38
+        src = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16)
+        src_np, sdt, sd = src.numpy().view(np.uint16), oracle.SRC_BF16, q.SRC_BF16
+    num_pages = 60
+    slots = rng.permutation(num_pages * 64)[:n].astype(np.int64)
+    slots[7] = -3
+    slots[8] = num_pages * 64 + 1             # out of the pool: skipped
+    pool = torch.full((num_pages, q.PAGE_BYTES_FP8_PER_TOKEN), 0x5A, dtype=torch.uint8, device="cuda")
+    q.kv_append_quant(src.cuda(), sd, torch.from_numpy(slots).cuda(), pool, None, q.KV_FP8_PER_TOKEN, 1.0)
+    torch.cuda.synchronize()
+    hp = np.full((num_pages, oracle.PAGE_BYTES_PT), 0x5A, np.uint8)
+    ok = slots < num_pages * 64
+    oracle.append(src_np[ok], sdt, slots[ok], oracle.KV_FP8_PT, 1.0, 64, num_pages, hp, None)
+    got = pool.cpu().numpy()
+    bad = np.nonzero((got != hp).any(1))[0]
+    assert bad.size == 0, f"{bad.size} pages differ, first {bad[:5]}"
+
+
 def test_append_workload_pool_matches_oracle(qkvp):
     """The NVFP4 pool of a decode workload, built through the library and by the oracle."""
     w = synth.build_workload("t", [700, 64, 1], heads=16, pool_pages=20, seed=3, outliers=4, device="cuda")

@@ -14,7 +14,7 @@ from tests.helpers import compare, gpu_decode, gpu_pools, oracle_decode, oracle_
 
 pytestmark = pytest.mark.gpu
 
-FP8, NVFP4, BF16 = q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_BF16
+FP8, NVFP4, BF16, FP8PT = q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_BF16, q.KV_FP8_PER_TOKEN
 
 
 def _run(w, kv, g=1.0, raw=False, **kw):
@@ -33,7 +33,7 @@ def test_tiny_workload(qkvp, kv):
 
 
 @pytest.mark.parametrize("heads", [16, 32, 48, 64, 128])
-@pytest.mark.parametrize("kv", [FP8, NVFP4, BF16])
+@pytest.mark.parametrize("kv", [FP8, NVFP4, BF16, FP8PT])
 def test_ragged_batch_many_splits(qkvp, heads, kv):
     lens = [1, 63, 64, 65, 200, 0, 1000, 4097, 129]
     w = synth.build_workload("ragged", lens, heads=heads, pool_pages=180, seed=heads + kv,
@@ -117,6 +117,8 @@ def _full_check(name, kv, g_mode="one", n_pairs=12, append=False, algo=0):
         lens = w.kv_len + 1
     if kv == NVFP4:
         assert np.array_equal(pools[0].cpu().numpy(), host[0]) and np.array_equal(pools[1].cpu().numpy(), host[1])
+    if kv == FP8PT:
+        assert np.array_equal(pools[0].cpu().numpy(), host[0])
     min_splits = 148 if w.batch == 1 else 0
     out, lse, plan = gpu_decode(w, kv, pools, g, min_splits=min_splits, lens=lens, algo=algo)
     assert torch.all(torch.isfinite(out.float())) and torch.all(torch.isfinite(lse))
@@ -131,6 +133,10 @@ def _full_check(name, kv, g_mode="one", n_pairs=12, append=False, algo=0):
 
 def test_full_fp8_b44_l32k(qkvp):
     _full_check("mla_fp8_b44_h128_l32k", FP8, algo=q.ALGO_MMA_SYNC)
+
+
+def test_full_fp8_per_token_b44_l32k(qkvp):
+    _full_check("mla_fp8_b44_h128_l32k", FP8PT, algo=q.ALGO_MMA_SYNC)
 
 
 def test_full_nvfp4_b10_l160k_with_append(qkvp):

@@ -12,7 +12,7 @@ from tests.test_gpu_decode import _full_check
 
 pytestmark = pytest.mark.gpu
 
-FP8, NVFP4, BF16 = q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_BF16
+FP8, NVFP4, BF16, FP8PT = q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_BF16, q.KV_FP8_PER_TOKEN
 TC = q.ALGO_TCGEN05
 
 
@@ -24,7 +24,7 @@ def _run(w, kv, g=1.0, raw=False, **kw):
     return stats, plan
 
 
-@pytest.mark.parametrize("kv", [FP8, NVFP4, BF16])
+@pytest.mark.parametrize("kv", [FP8, NVFP4, BF16, FP8PT])
 def test_tc_ragged_batch_many_splits(qkvp, kv):
     lens = [1, 63, 64, 65, 200, 0, 1000, 4097, 129]
     w = synth.build_workload("ragged", lens, heads=128, pool_pages=180, seed=40 + kv, outliers=4,
@@ -73,6 +73,10 @@ def test_tc_matches_mma_kernel(qkvp):
 
 def test_tc_full_fp8_b44_l32k(qkvp):
     _full_check("mla_fp8_b44_h128_l32k", FP8, algo=TC)
+
+
+def test_tc_full_fp8_per_token_b44_l32k(qkvp):
+    _full_check("mla_fp8_b44_h128_l32k", FP8PT, algo=TC)
 
 
 def test_tc_full_nvfp4_b10_l160k_with_append(qkvp):
