@@ -81,7 +81,9 @@ typedef enum { QKVP_SRC_FP8_E4M3 = 1, QKVP_SRC_BF16 = 2 } qkvp_src_dtype;
 typedef enum {
   QKVP_ALGO_AUTO = 0,
   QKVP_ALGO_MMA_SYNC = 1,  /* warp-level mma.sync split-KV kernel, any supported head count */
-  QKVP_ALGO_TCGEN05 = 2    /* tcgen05/TMEM CTA-pair split-KV kernel, 128 heads (AUTO picks it) */
+  QKVP_ALGO_TCGEN05 = 2    /* tcgen05/TMEM CTA-pair split-KV kernel: always 128 head rows (fewer heads
+                              ride as zero rows), so its cost does not shrink with the heads; AUTO picks
+                              it at 64 heads and more, the mma.sync kernel below */
 } qkvp_algo;
 
 #define QKVP_LATENT_DIM 576

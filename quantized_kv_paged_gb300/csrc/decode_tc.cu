@@ -530,9 +530,12 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       // ---- Q row of head h (QK of the previous page has completed: its logits were read). A
       // power of two 2^-sh from the row's largest |q| (the same in both CTAs) keeps every value
       // inside FP16; 2^sh joins this row's logit scale ----
-      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(seg.req) * 128 + h) * (kLatent * 2);
+      // With fewer than 128 query heads the rows h >= heads hold zeros: their logits are 0, their
+      // softmax runs on them harmlessly and nothing of theirs is written.
+      const bool live = h < a.heads;
+      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(seg.req) * a.heads + (live ? h : 0)) * (kLatent * 2);
       uint32_t mx = 0;
-      for (int i = 0; i < kLatent * 2 / 16; ++i) {
+      for (int i = 0; live && i < kLatent * 2 / 16; ++i) {
         const uint4 v = *reinterpret_cast<const uint4*>(qrow + 16 * i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -550,7 +553,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
         const uint8_t* src = qrow + perm(64 * part) * 2;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + 16 * i);
+          const uint4 v = live ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
           r[4 * i] = dev::bf16x2_to_f16x2(v.x, down);
           r[4 * i + 1] = dev::bf16x2_to_f16x2(v.y, down);
           r[4 * i + 2] = dev::bf16x2_to_f16x2(v.z, down);
@@ -561,7 +564,8 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       }
 #pragma unroll
       for (int i = 0; i < 8 * kQSmemAtoms; ++i) {     // positions 384..575 -> 64-dim atoms, row h
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + (perm(kQTmemDims + 64 * (i >> 3)) + 8 * (i & 7)) * 2);
+        const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + (perm(kQTmemDims + 64 * (i >> 3)) + 8 * (i & 7)) * 2)
+                             : make_uint4(0, 0, 0, 0);
         sts128(qs + (i >> 3) * kQAtom + tc::sw128_offset(h, i & 7),
                make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
                           dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
@@ -728,6 +732,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       uint32_t orow[32];
       tc::tmem_ld32(tl + TM_O + 32 * cc, orow);
       tc::tmem_wait_ld();
+      if (h >= a.heads) continue;            // a padding row (the TMEM load above is warp-wide)
       if (seg.partial < 0) {
         const float sc = inv * a.out_scale;
         uint4* dst = reinterpret_cast<uint4*>(a.out + row * kDv + 256 * c + 32 * cc);
@@ -746,7 +751,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       }
     }
     tc::tc_fence_before();
-    if (c == 0) {
+    if (c == 0 && h < a.heads) {
       if (seg.partial < 0) { if (a.lse) a.lse[row] = lse2 * 0.69314718055994531f; }
       else a.part_lse[static_cast<int64_t>(seg.partial) * a.heads + h] = lse2;
     }
@@ -864,7 +869,7 @@ int tc_max_active_clusters() {
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {
   if (a.num_segments == 0) return cudaSuccess;
-  if (a.heads != 128 || a.ctas_per_worker != 2) return cudaErrorInvalidValue;
+  if (a.heads < 16 || a.heads > 128 || a.heads % 16 || a.ctas_per_worker != 2) return cudaErrorInvalidValue;
   switch (a.kv_dtype) {
     case KV_FP8: return launch_kv<KV_FP8>(a, s);
     case KV_NVFP4: return launch_kv<KV_NVFP4>(a, s);

@@ -58,6 +58,10 @@ def test_plan_rejects_bad_arguments(lib):
     assert plan(np.array([0, 2, 1], np.int32), np.array([5, 5], np.int32)).status == q.QKVP_E_INVALID
     assert plan(ok_ptr, ok_len, min_splits=-1).status == q.QKVP_E_INVALID
     assert plan(ok_ptr, ok_len, algo=7).status == q.QKVP_E_UNSUPPORTED
+    # AUTO: the tcgen05 kernel from 64 heads up (it always computes 128 head rows), mma.sync below
+    assert plan(ok_ptr, ok_len, heads=64).algo == q.ALGO_TCGEN05
+    assert plan(ok_ptr, ok_len, heads=48).algo == q.ALGO_MMA_SYNC
+    assert plan(ok_ptr, ok_len, heads=16, algo=q.ALGO_TCGEN05).status == q.QKVP_OK
 
 
 def test_plan_workspace_too_small_reports_size(lib):

@@ -34,6 +34,16 @@ def test_tc_ragged_batch_many_splits(qkvp, kv):
         assert plan.algo == TC and plan.ctas_per_worker == 2
 
 
+@pytest.mark.parametrize("heads", [16, 64, 96])
+def test_tc_fewer_heads_ride_as_zero_rows(qkvp, heads):
+    lens = [1, 65, 200, 0, 1000, 4097]
+    w = synth.build_workload("few", lens, heads=heads, pool_pages=120, seed=heads, outliers=4, device="cuda",
+                             extra_pages=[1] * len(lens))
+    for kv in (FP8, NVFP4):
+        stats, plan = _run(w, kv, g=1.0 if kv != NVFP4 else 0.37, num_sms=37)
+        assert plan.algo == TC
+
+
 def test_tc_tiny_single_page(qkvp):
     w = synth.build_workload("one", [17], heads=128, pool_pages=3, seed=3, device="cuda")
     _run(w, FP8, raw=True, num_sms=2)
