@@ -23,8 +23,10 @@
 //   cp.async raw page -> smem  |  dequantize -> FP16 tile [64 tokens][576]  |  S = Q K^T (mma.sync)
 //   |  exchange + online softmax (FP32, base 2)  |  O += P V (mma.sync, P from registers).
 // The next page's raw bytes are fetched while the current page is multiplied.
+#include <cuda.h>          // CUtensorMap and the tensor-map encoder's types (fetched from the driver at run time)
 #include <cfloat>
 #include <cstdint>
+#include <cstring>
 
 #include "qkvp_device.cuh"
 #include "qkvp_internal.h"
@@ -37,11 +39,34 @@ constexpr int kRow = kLatent + 8;          // padded smem row of the 16-bit tile
 constexpr int kRowBytes = kRow * 2;
 constexpr int kSigByte = kLatent * 2;      // a per-token-scaled page keeps the token's scale here
 
+// FP8 pools take the raw-operand path: no dequantized tile. A page's stored bytes are brought into
+// shared memory by four tensor-map loads (TMA), one per 144-dim column box, each box laid out as 64
+// rows of 144 bytes: byte (token t, dim d) sits at (d / 144) * 9216 + 144 t + d % 144. A 144-byte
+// pitch is nine 16-byte bank groups (an odd number), so eight rows fall in eight distinct groups
+// whenever their token indices differ mod 8. K fragments come from a plain ldmatrix of the bytes (4
+// consecutive dims per lane: two E4M3 pairs, converted exactly to the two F16x2 registers of an
+// m16n8k16 B fragment under a fixed permutation of the contraction dims, which Q's shared-memory copy
+// follows), V fragments from the transposing byte ldmatrix (4 consecutive rows per lane: the P.V B
+// fragment under a token permutation that the Q.K^T output columns follow, so P passes from the
+// logit registers into the A fragments unchanged). Within each 16-token tile, row r of those loads is
+// token rho(r) = r ^ 2 for r >= 8 (r below 8): with it, the 8 tokens of every ldmatrix phase are
+// distinct mod 8.
+template <int KV>
+constexpr bool raw_operands() { return KV == KV_FP8 || KV == KV_FP8PT; }
+constexpr int kBoxDims = 144;                        // dims per TMA box
+constexpr int kBoxBytes = kPage * kBoxDims;          // 9,216
+constexpr int kRawRows = 4 * kBoxBytes;              // 36,864; a per-token-scaled page's scales follow
+__host__ __device__ constexpr int rho(int r) { return r ^ ((r >> 2) & 2); }
+// byte offset of the 16-dim chunk c (0..35) of token row t
+__host__ __device__ constexpr int raw_chunk_off(int t, int c) { return (c / 9) * kBoxBytes + t * kBoxDims + (c % 9) * 16; }
+
 template <int KV>
 constexpr int raw_bytes() {
-  return KV == KV_FP8 ? kPage * kLatent
-       : KV == KV_NVFP4 ? kPage * (kPacked + kScales) : KV == KV_FP8PT ? kPtPageBytes : 0;
+  return KV == KV_FP8 ? kRawRows
+       : KV == KV_NVFP4 ? kPage * (kPacked + kScales) : KV == KV_FP8PT ? kRawRows + 4 * kPage : 0;
 }
+template <int KV>
+constexpr int tile_bytes() { return raw_operands<KV>() ? 0 : kPage * kRowBytes; }
 
 constexpr int kNT = 256;                   // threads per CTA: every warp dequantizes
 
@@ -49,15 +74,17 @@ constexpr int kNT = 256;                   // threads per CTA: every warp dequan
 template <int HC>
 constexpr int pairs() { return (HC / 16) * ((HC / 16) >= 3 ? 1 : 4 / (HC / 16)); }
 
-// Raw page buffers: two (pages fetched two ahead) unless that overflows shared memory (64 heads).
+// Raw page buffers: as many as fit up to three (pages fetched that far ahead), at least one.
 template <int KV, int HC>
 constexpr int raw_bufs() {
-  return KV == KV_BF16 ? 0 : (HC * kRowBytes + kPage * kRowBytes + 2 * raw_bytes<KV>() + pairs<HC>() * 8192 + 64 <= 232448 - 1024 ? 2 : 1);
+  return KV == KV_BF16 ? 0
+       : HC * kRowBytes + tile_bytes<KV>() + 3 * raw_bytes<KV>() + pairs<HC>() * 8192 + 64 <= 232448 - 1024 ? 3
+       : HC * kRowBytes + tile_bytes<KV>() + 2 * raw_bytes<KV>() + pairs<HC>() * 8192 + 64 <= 232448 - 1024 ? 2 : 1;
 }
 
 template <int KV, int HC>
 constexpr int smem_bytes() {
-  return HC * kRowBytes + kPage * kRowBytes + raw_bufs<KV, HC>() * raw_bytes<KV>() + pairs<HC>() * 2 * 32 * 32 * 4 + 64;
+  return HC * kRowBytes + tile_bytes<KV>() + raw_bufs<KV, HC>() * raw_bytes<KV>() + pairs<HC>() * 2 * 32 * 32 * 4 + 64;
 }
 
 // Raw bytes of one page (FP8, per-token-scaled FP8: the page; NVFP4: data then block scales) into a
@@ -78,6 +105,23 @@ __device__ __forceinline__ void fetch_page(const DecodeArgs& a, int64_t page, ui
     tc::bulk_load(s_raw, a.kv + page * (kPage * kPacked), kPage * kPacked, bar);
     tc::bulk_load(s_raw + kPage * kPacked, a.kv_scale + page * (kPage * kScales), kPage * kScales, bar);
   }
+}
+
+// Raw-operand path: the page's 64 rows as four 144-dim boxes (and a per-token-scaled page's 64 scales)
+// into a raw buffer, counted on `bar` by one expect-tx arrival of the issuing thread. Rows past the
+// page's tokens come along and are zeroed after the wait. A page id outside the pool copies nothing;
+// the arrival alone completes the phase.
+template <int KV>
+__device__ __forceinline__ void fetch_raw_page(const DecodeArgs& a, const CUtensorMap* map, int64_t page,
+                                               uint32_t s_raw, uint32_t bar) {
+  if (page < 0 || page >= a.num_pages) {
+    tc::mbar_arrive(bar);
+    return;
+  }
+  tc::mbar_arrive_expect_tx(bar, raw_bytes<KV>());
+#pragma unroll
+  for (int b = 0; b < 4; ++b) tc::tma_load_3d(s_raw + b * kBoxBytes, map, b * kBoxDims, 0, static_cast<int>(page), bar);
+  if (KV == KV_FP8PT) tc::bulk_load(s_raw + kRawRows, a.kv + page * kPtPageBytes + kPtScaleOff, 4 * kPage, bar);
 }
 
 // Fetch the raw bytes of one page (or, for BF16, the page itself) with cp.async.
@@ -181,7 +225,7 @@ __device__ __forceinline__ void dequant_page(const uint8_t* s_raw, uint8_t* s_kv
 }
 
 template <int KV, int HC>
-__global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kv_map) {
   constexpr int NG = HC / 16;       // 16-head groups in this CTA
   // With few heads the page's 64 tokens are split among warp pairs too, so that all 8 warps do
   // math: TG token groups of TPG tokens, each pair with its own softmax state, merged at the end
@@ -193,10 +237,11 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
   constexpr int NT = kNT;
   constexpr int NB = raw_bufs<KV, HC>();
   constexpr int NBx = NB > 0 ? NB : 1;
+  constexpr bool RAW = raw_operands<KV>();
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_q = smem;
-  uint8_t* s_kv = s_q + HC * kRowBytes;
-  uint8_t* s_raw = s_kv + kPage * kRowBytes;
+  uint8_t* s_kv = s_q + HC * kRowBytes;      // the dequantized page tile (not on the raw-operand path)
+  uint8_t* s_raw = s_kv + tile_bytes<KV>();
   float* s_x = reinterpret_cast<float*>(s_raw + NB * raw_bytes<KV>());
   uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + NPAIR * 2 * 1024);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_qmax + 2);          // NB FULL barriers (8-byte aligned)
@@ -260,12 +305,26 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
       if (qm != 0u && qm < 0x7F80u) sh = max(-100, min(113, static_cast<int>(qm >> 7) - 127 - 14));
       const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
       q_scale_log2 = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
-      for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
-        const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
-        uint4* p = reinterpret_cast<uint4*>(s_q + row * kRowBytes + ch * 16);
-        const uint4 v = *p;
-        *p = make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
-                        dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down));
+      if constexpr (RAW) {
+        // raw-operand path: within every 16 dims, position 2a + e holds dim 4a + e and position
+        // 8 + 2a + e holds dim 4a + 2 + e (a < 4, e < 2), the order a lane's K fragment bytes come in
+        for (int c = tid; c < HC * (kLatent / 16); c += NT) {
+          const int row = c / (kLatent / 16), ch = c % (kLatent / 16);
+          uint4* p = reinterpret_cast<uint4*>(s_q + row * kRowBytes + ch * 32);
+          const uint4 v0 = p[0], v1 = p[1];
+          p[0] = make_uint4(dev::bf16x2_to_f16x2(v0.x, down), dev::bf16x2_to_f16x2(v0.z, down),
+                            dev::bf16x2_to_f16x2(v1.x, down), dev::bf16x2_to_f16x2(v1.z, down));
+          p[1] = make_uint4(dev::bf16x2_to_f16x2(v0.y, down), dev::bf16x2_to_f16x2(v0.w, down),
+                            dev::bf16x2_to_f16x2(v1.y, down), dev::bf16x2_to_f16x2(v1.w, down));
+        }
+      } else {
+        for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
+          const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
+          uint4* p = reinterpret_cast<uint4*>(s_q + row * kRowBytes + ch * 16);
+          const uint4 v = *p;
+          *p = make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
+                          dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down));
+        }
       }
       cur_req = seg.req;
       // the conversion is made visible to every warp by the barrier before the first page
@@ -275,8 +334,13 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
     for (int i = 0; i < 32; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.0f, 0.0f};
 
-    // raw pages of this segment stream in NB ahead of the page being dequantized
-    if (KV != KV_BF16 && tid == 0) {
+    // raw pages of this segment stream in NB ahead of the page being used
+    if constexpr (RAW) {
+      if (tid == 0) {
+        for (int k = 0; k < NB && k < seg.num_pages; ++k)
+          fetch_raw_page<KV>(a, &kv_map, a.kv_indices[seg.page_begin + k], a_raw + k * raw_bytes<KV>(), a_bar + 8 * k);
+      }
+    } else if (KV != KV_BF16 && tid == 0) {
       for (int k = 0; k < NB && k < seg.num_pages; ++k)
         fetch_page<KV>(a, a.kv_indices[seg.page_begin + k], a_raw + k * raw_bytes<KV>(), a_bar + 8 * k);
     }
@@ -295,21 +359,70 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
         }
         ++fills[buf];
       }
-      __syncthreads();
-      dequant_page<KV, NT>(s_raw + buf * raw_bytes<KV>(), s_kv, page_ok ? valid : 0, tid);
-      __syncthreads();
-      if (j + 1 < seg.num_pages) page = a.kv_indices[seg.page_begin + j + 1];
-      if (KV != KV_BF16 && tid == 0 && j + NB < seg.num_pages) {
-        tc::fence_proxy_async_smem();   // this buffer's reads are done before the copy refills it
-        fetch_page<KV>(a, a.kv_indices[seg.page_begin + j + NB], a_raw + buf * raw_bytes<KV>(), a_bar + 8 * buf);
-      }
       const int live = page_ok ? valid : 0;
+      uint8_t* rbuf = s_raw + buf * raw_bytes<KV>();
+      const uint32_t a_rb = a_raw + buf * raw_bytes<KV>();
+      if constexpr (RAW) {
+        // rows past the page's tokens (and their scales) read as zeros: P is 0 there, and V must not
+        // bring NaN codes into P.V
+        if (live < kPage) {
+          for (int c = tid; c < (kPage - live) * (kLatent / 16); c += NT) {
+            const int t = live + c / (kLatent / 16), ch = c % (kLatent / 16);
+            *reinterpret_cast<uint4*>(rbuf + raw_chunk_off(t, ch)) = make_uint4(0, 0, 0, 0);
+          }
+          if (KV == KV_FP8PT)
+            for (int t = live + tid; t < kPage; t += NT) reinterpret_cast<float*>(rbuf + kRawRows)[t] = 0.0f;
+        }
+        __syncthreads();
+        if (j + 1 < seg.num_pages) page = a.kv_indices[seg.page_begin + j + 1];
+      } else {
+        __syncthreads();
+        dequant_page<KV, NT>(rbuf, s_kv, live, tid);
+        __syncthreads();
+        if (j + 1 < seg.num_pages) page = a.kv_indices[seg.page_begin + j + 1];
+        if (KV != KV_BF16 && tid == 0 && j + NB < seg.num_pages) {
+          tc::fence_proxy_async_smem();   // this buffer's reads are done before the copy refills it
+          fetch_page<KV>(a, a.kv_indices[seg.page_begin + j + NB], a_rb, a_bar + 8 * buf);
+        }
+      }
       if (mma_warp) {
 
       // ---- S partial = Q[:, my dims] K[my tokens, my dims]^T  (16 heads x TPG tokens) ----
       float s[2 * NP][4];
 #pragma unroll
       for (int n = 0; n < 2 * NP; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
+      if constexpr (RAW) {
+        // K fragments straight from the page bytes: per 16-token tile p and n8 tile jj, lane l
+        // addresses tile row rho(4((l & 7) >> 1) + (l & 1) + 2jj), k-step (l >> 3) of a block of
+        // four; it receives dims 4t4 .. 4t4+3 of the row of logit column g8, i.e. B[2t4, 2t4+1] and
+        // B[8 + 2t4, 9 + 2t4] in Q's permuted dim order
+        const int kr = lane & 7;
+#pragma unroll
+        for (int kb = 0; kb < 5; ++kb) {       // k-steps 4kb .. 4kb + 3 (two in the last block)
+          constexpr int kSteps = 18;
+          uint32_t aq[4][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (4 * kb + i < kSteps)
+              dev::ldsm_x4(a_q + q_lane + (half * 288 + 16 * (4 * kb + i)) * 2, aq[i][0], aq[i][1], aq[i][2], aq[i][3]);
+#pragma unroll
+          for (int p = 0; p < NP; ++p)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const uint32_t addr = a_rb + raw_chunk_off(t0 + 16 * p + rho(4 * (kr >> 1) + (kr & 1) + 2 * jj),
+                                                         half * 18 + 4 * kb + (lane >> 3));
+              uint32_t r[4];
+              if (kb < 4) dev::ldsm_x4(addr, r[0], r[1], r[2], r[3]);
+              else dev::ldsm_x2(addr, r[0], r[1]);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (4 * kb + i < kSteps)
+                  dev::mma_f16(s[2 * p + jj], aq[i][0], aq[i][1], aq[i][2], aq[i][3],
+                               dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r[i] & 0xFFFFu)),
+                               dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r[i] >> 16)));
+            }
+        }
+      } else {
 #pragma unroll 2
       for (int ks = 0; ks < 18; ++ks) {
         const int kk = half * 288 + ks * 16;
@@ -322,6 +435,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
           dev::mma_f16(s[2 * p], a0, a1, a2, a3, b0, b1);
           dev::mma_f16(s[2 * p + 1], a0, a1, a2, a3, b2, b3);
         }
+      }
       }
       // ---- exchange the partial logits with the peer warp; sum in a fixed order ----
 #pragma unroll
@@ -338,19 +452,25 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
         }
       // ---- online softmax in base 2 (rows g8 and g8 + 8 of the 16 heads) ----
       // per-token-scaled pages: the token scale multiplies the logit and the probability (not l)
+      // page token of logit column 2t4 + e of n8 tile n: on the raw-operand path tile 2p + jj holds
+      // tile rows {0,1,4,5,8,9,12,13} + 2jj (the order the P.V B fragments take them in), through rho
+      auto tok_of = [&](int n, int e) {
+        return RAW ? t0 + 16 * (n >> 1) + rho(4 * t4 + e + 2 * (n & 1)) : t0 + n * 8 + 2 * t4 + e;
+      };
       float sig[2 * NP][2];
 #pragma unroll
       for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
-          sig[n][e] = KV == KV_FP8PT
-              ? *reinterpret_cast<const float*>(s_kv + (t0 + n * 8 + 2 * t4 + e) * kRowBytes + kSigByte) : 1.0f;
+          sig[n][e] = KV != KV_FP8PT ? 1.0f
+              : RAW ? reinterpret_cast<const float*>(rbuf + kRawRows)[tok_of(n, e)]
+                    : *reinterpret_cast<const float*>(s_kv + tok_of(n, e) * kRowBytes + kSigByte);
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int n = 0; n < 2 * NP; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int tok = t0 + n * 8 + 2 * t4 + (i & 1);
+          const int tok = tok_of(n, i & 1);
           const float x = KV == KV_FP8PT ? s[n][i] * sig[n][i & 1] : s[n][i];
           const float v = tok < live ? x * q_scale_log2 : -INFINITY;
           s[n][i] = v;
@@ -389,6 +509,21 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
         const uint32_t pa1 = dev::pack_f16x2(s[2 * kt][2] * sa[0], s[2 * kt][3] * sa[1]);
         const uint32_t pa2 = dev::pack_f16x2(s[2 * kt + 1][0] * sb[0], s[2 * kt + 1][1] * sb[1]);
         const uint32_t pa3 = dev::pack_f16x2(s[2 * kt + 1][2] * sb[0], s[2 * kt + 1][3] * sb[1]);
+        if constexpr (RAW) {
+          // V fragments straight from the page bytes: lanes 0..15 address the tile's 16 rows (token
+          // rho(r) for row r) at a 16-dim block, lanes 16..31 at the next block; each lane receives
+          // rows 4t4 .. 4t4+3 (P's k order above) of dims g8 and 8 + g8 of each block
+          const int vt = t0 + kt * 16 + rho(lane & 15);
+#pragma unroll
+          for (int vq = 0; vq < 8; ++vq) {
+            uint32_t r[4];
+            dev::ldsm_t8_x2(a_rb + raw_chunk_off(vt, half * 16 + 2 * vq + (lane >> 4)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dev::mma_f16(o[4 * vq + u], pa0, pa1, pa2, pa3, dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r[u] & 0xFFFFu)),
+                           dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r[u] >> 16)));
+          }
+        } else {
 #pragma unroll
         for (int vp = 0; vp < 16; ++vp) {
           uint32_t b0, b1, b2, b3;
@@ -396,9 +531,17 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
           dev::mma_f16(o[2 * vp], pa0, pa1, pa2, pa3, b0, b1);
           dev::mma_f16(o[2 * vp + 1], pa0, pa1, pa2, pa3, b2, b3);
         }
+        }
       }
       }
       __syncthreads();  // s_kv and the exchange buffers are reused by the next page
+      if constexpr (RAW) {
+        // every warp is done with this buffer: it takes page j + NB
+        if (tid == 0 && j + NB < seg.num_pages) {
+          tc::fence_proxy_async_smem();
+          fetch_raw_page<KV>(a, &kv_map, a.kv_indices[seg.page_begin + j + NB], a_rb, a_bar + 8 * buf);
+        }
+      }
     }
     if (!mma_warp) continue;
 
@@ -414,7 +557,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
       // (O, m, l) in their fragment order, the tg = 0 pair of the same heads reads them back
       float* mrg = reinterpret_cast<float*>(s_kv);
       constexpr int kSlot = 32 * 128 + 32 * 4;            // one warp's O fragments, then m and l
-      static_assert(NG * (TG - 1) * 2 * kSlot * 4 <= kPage * kRowBytes + NB * raw_bytes<KV>() + NPAIR * 8192,
+      static_assert(NG * (TG - 1) * 2 * kSlot * 4 <= tile_bytes<KV>() + NB * raw_bytes<KV>() + NPAIR * 8192,
                     "merge slots fit in the page tile, raw buffers and exchange buffers");
       auto slot = [&](int g, int t, int hf) { return mrg + ((g * (TG - 1) + (t - 1)) * 2 + hf) * kSlot; };
       if (tg > 0) {
@@ -475,6 +618,33 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a) 
   }
 }
 
+// The pool as a 3-D tensor of bytes {576 dims, 64 tokens, pages} (page stride 36,864 or 37,120) for
+// the raw-operand path's TMA loads: box {144, 64, 1}, no swizzle, no interleave.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encode_kv_map(const DecodeArgs& a, int64_t page_bytes, CUtensorMap* map) {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+      return cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kLatent), static_cast<cuuint64_t>(kPage),
+                              static_cast<cuuint64_t>(a.num_pages)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kLatent), static_cast<cuuint64_t>(page_bytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxDims), static_cast<cuuint32_t>(kPage), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.kv), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int KV, int HC>
 cudaError_t launch_kv_hc(const DecodeArgs& a, cudaStream_t s) {
   constexpr int smem = smem_bytes<KV, HC>();
@@ -484,8 +654,14 @@ cudaError_t launch_kv_hc(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (raw_operands<KV>() && a.num_pages > 0) {
+    const cudaError_t e = encode_kv_map(a, KV == KV_FP8PT ? kPtPageBytes : kPage * kLatent, &map);
+    if (e != cudaSuccess) return e;
+  }
   const unsigned grid = static_cast<unsigned>(a.num_workers * a.ctas_per_worker);
-  decode_mma_kernel<KV, HC><<<grid, kNT, smem, s>>>(a);
+  decode_mma_kernel<KV, HC><<<grid, kNT, smem, s>>>(a, map);
   return cudaGetLastError();
 }
 

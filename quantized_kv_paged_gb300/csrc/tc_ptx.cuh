@@ -139,6 +139,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, ui
                :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Tiled tensor load (TMA) of one box of a 3-D tensor map into shared memory, counted on `bar`. The
+// innermost coordinate x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const void* tmap, int x, int y, int z, uint32_t bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(dst_smem), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+
 // Asynchronous bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
 // CTA's shared memory to the same offset in CTA `rank` of the cluster; completion is counted in
 // bytes on the mbarrier at offset `bar_local` of that CTA.
