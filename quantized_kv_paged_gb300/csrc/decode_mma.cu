@@ -74,17 +74,22 @@ constexpr int kNT = 256;                   // threads per CTA: every warp dequan
 template <int HC>
 constexpr int pairs() { return (HC / 16) * ((HC / 16) >= 3 ? 1 : 4 / (HC / 16)); }
 
+// Logit exchange buffers: 4 KB per warp, two sets (alternate pages) on the raw-operand path, whose
+// warps run without a CTA-wide barrier per page.
+template <int KV, int HC>
+constexpr int xbuf_bytes() { return pairs<HC>() * 8192 * (raw_operands<KV>() ? 2 : 1); }
+
 // Raw page buffers: as many as fit up to three (pages fetched that far ahead), at least one.
 template <int KV, int HC>
 constexpr int raw_bufs() {
   return KV == KV_BF16 ? 0
-       : HC * kRowBytes + tile_bytes<KV>() + 3 * raw_bytes<KV>() + pairs<HC>() * 8192 + 64 <= 232448 - 1024 ? 3
-       : HC * kRowBytes + tile_bytes<KV>() + 2 * raw_bytes<KV>() + pairs<HC>() * 8192 + 64 <= 232448 - 1024 ? 2 : 1;
+       : HC * kRowBytes + tile_bytes<KV>() + 3 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 3
+       : HC * kRowBytes + tile_bytes<KV>() + 2 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 2 : 1;
 }
 
 template <int KV, int HC>
 constexpr int smem_bytes() {
-  return HC * kRowBytes + tile_bytes<KV>() + raw_bufs<KV, HC>() * raw_bytes<KV>() + pairs<HC>() * 2 * 32 * 32 * 4 + 64;
+  return HC * kRowBytes + tile_bytes<KV>() + raw_bufs<KV, HC>() * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64;
 }
 
 // Raw bytes of one page (FP8, per-token-scaled FP8: the page; NVFP4: data then block scales) into a
@@ -243,8 +248,9 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
   uint8_t* s_kv = s_q + HC * kRowBytes;      // the dequantized page tile (not on the raw-operand path)
   uint8_t* s_raw = s_kv + tile_bytes<KV>();
   float* s_x = reinterpret_cast<float*>(s_raw + NB * raw_bytes<KV>());
-  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + NPAIR * 2 * 1024);
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_qmax + 2);          // NB FULL barriers (8-byte aligned)
+  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + NPAIR * 2 * 1024 * (RAW ? 2 : 1));
+  // NB FULL barriers, then (raw-operand path) NB EMPTY barriers: 8-byte aligned
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_qmax + 2);
   const uint32_t a_q = dev::smem_u32(s_q), a_kv = dev::smem_u32(s_kv), a_raw = dev::smem_u32(s_raw);
   const uint32_t a_bar = dev::smem_u32(s_bar);
 
@@ -259,6 +265,8 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
   const bool mma_warp = warp < 2 * NPAIR;
   if (KV != KV_BF16 && tid == 0) {
     for (int b = 0; b < NB; ++b) tc::mbar_init(a_bar + 8 * b, 1);
+    if (RAW)
+      for (int b = 0; b < NB; ++b) tc::mbar_init(a_bar + 8 * (NB + b), NT / 32);   // one arrival per warp
     tc::fence_mbar_init();
   }
   int fills[NBx];                   // completed phases of each raw buffer's barrier
@@ -269,8 +277,8 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
   const uint32_t q_lane = ((grp * 16 + (lane & 15)) * kRow + (lane >> 4) * 8) * 2;
   const uint32_t k_lane = (((lane & 7) + ((lane >> 4) << 3)) * kRow + ((lane >> 3) & 1) * 8) * 2;
   const uint32_t v_lane = (((lane & 7) + ((lane >> 3) & 1) * 8) * kRow + half * 256 + (lane >> 4) * 8) * 2;
-  float* x_mine = s_x + (pi * 2 + half) * 1024;
-  float* x_peer = s_x + (pi * 2 + (half ^ 1)) * 1024;
+  float* const x_mine0 = s_x + (pi * 2 + half) * 1024;
+  float* const x_peer0 = s_x + (pi * 2 + (half ^ 1)) * 1024;
 
   int cur_req = -1;
   float q_scale_log2 = a.scale_log2;
@@ -349,6 +357,15 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       const int valid = min(kPage, seg.num_tokens - j * kPage);
       const bool page_ok = page >= 0 && page < a.num_pages;
       const int buf = NB > 0 ? j % NB : 0;
+      if (RAW && tid == 0 && j >= 1 && j - 1 + NB < seg.num_pages) {
+        // the buffer of page j - 1 takes page j - 1 + NB once every warp is done with page j - 1
+        // (its fills[]-th use: EMPTY completes once per use)
+        const int pb = (j - 1) % NB;
+        if (!tc::mbar_wait(a_bar + 8 * (NB + pb), (fills[pb] - 1) & 1)) atomicOr(a.status, 16);
+        tc::fence_proxy_async_smem();
+        fetch_raw_page<KV>(a, &kv_map, a.kv_indices[seg.page_begin + j - 1 + NB], a_raw + pb * raw_bytes<KV>(),
+                           a_bar + 8 * pb);
+      }
       if (KV == KV_BF16) {
         issue_page<KV, NT>(a, page, valid, a_raw, a_kv, tid);
         dev::cp_async_wait_all();
@@ -362,6 +379,10 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       const int live = page_ok ? valid : 0;
       uint8_t* rbuf = s_raw + buf * raw_bytes<KV>();
       const uint32_t a_rb = a_raw + buf * raw_bytes<KV>();
+      // logit exchange buffers of this page (two sets on the raw-operand path: a warp may write page
+      // j + 1's while its peer still reads page j's; page j + 2 waits for the pair barrier of j + 1)
+      float* x_mine = x_mine0 + (RAW && (j & 1) ? NPAIR * 2 * 1024 : 0);
+      float* x_peer = x_peer0 + (RAW && (j & 1) ? NPAIR * 2 * 1024 : 0);
       if constexpr (RAW) {
         // rows past the page's tokens (and their scales) read as zeros: P is 0 there, and V must not
         // bring NaN codes into P.V
@@ -372,8 +393,8 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
           }
           if (KV == KV_FP8PT)
             for (int t = live + tid; t < kPage; t += NT) reinterpret_cast<float*>(rbuf + kRawRows)[t] = 0.0f;
+          __syncthreads();
         }
-        __syncthreads();
         if (j + 1 < seg.num_pages) page = a.kv_indices[seg.page_begin + j + 1];
       } else {
         __syncthreads();
@@ -397,6 +418,12 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         // four; it receives dims 4t4 .. 4t4+3 of the row of logit column g8, i.e. B[2t4, 2t4+1] and
         // B[8 + 2t4, 9 + 2t4] in Q's permuted dim order
         const int kr = lane & 7;
+        // with one or two 16-token tiles, odd k-steps accumulate apart: twice the independent
+        // chains of dependent MMAs (four tiles have enough already)
+        constexpr bool kSplit = NP <= 2;
+        float s2[kSplit ? 2 * NP : 1][4];
+#pragma unroll
+        for (int n = 0; n < (kSplit ? 2 * NP : 1); ++n) s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.0f;
 #pragma unroll
         for (int kb = 0; kb < 5; ++kb) {       // k-steps 4kb .. 4kb + 3 (two in the last block)
           constexpr int kSteps = 18;
@@ -417,10 +444,16 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 if (4 * kb + i < kSteps)
-                  dev::mma_f16(s[2 * p + jj], aq[i][0], aq[i][1], aq[i][2], aq[i][3],
+                  dev::mma_f16((kSplit && (i & 1)) ? s2[kSplit ? 2 * p + jj : 0] : s[2 * p + jj], aq[i][0], aq[i][1], aq[i][2], aq[i][3],
                                dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r[i] & 0xFFFFu)),
                                dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r[i] >> 16)));
             }
+        }
+        if constexpr (kSplit) {
+#pragma unroll
+          for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[n][i] += s2[n][i];
         }
       } else {
 #pragma unroll 2
@@ -534,15 +567,17 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         }
       }
       }
-      __syncthreads();  // s_kv and the exchange buffers are reused by the next page
       if constexpr (RAW) {
-        // every warp is done with this buffer: it takes page j + NB
-        if (tid == 0 && j + NB < seg.num_pages) {
-          tc::fence_proxy_async_smem();
-          fetch_raw_page<KV>(a, &kv_map, a.kv_indices[seg.page_begin + j + NB], a_rb, a_bar + 8 * buf);
-        }
+        // this warp is done with the page's buffer
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(a_bar + 8 * (NB + buf));
+      } else {
+        __syncthreads();  // s_kv and the exchange buffers are reused by the next page
       }
     }
+    // raw-operand path: every warp is done with the segment's pages (the merge below reuses the raw
+    // buffers) and no copy is in flight (the last pages were consumed)
+    if constexpr (RAW) __syncthreads();
     if (!mma_warp) continue;
 
     // ---- epilogue: normalise; write the output directly or a split partial ----
