@@ -51,11 +51,16 @@ constexpr int kSigByte = kLatent * 2;      // a per-token-scaled page keeps the 
 // logit registers into the A fragments unchanged). Within each 16-token tile, row r of those loads is
 // token rho(r) = r ^ 2 for r >= 8 (r below 8): with it, the 8 tokens of every ldmatrix phase are
 // distinct mod 8.
-template <int KV>
-constexpr bool raw_operands() { return KV == KV_FP8 || KV == KV_FP8PT; }
+// FP8 pools take it at every head count; NVFP4 pools only at 16 heads per CTA: with more head groups
+// each group would unpack and scale the same codes again (the FP8 conversion is one instruction per
+// pair, the NVFP4 one several), and one shared dequantized tile is cheaper.
+template <int KV, int HC>
+constexpr bool raw_operands() { return KV == KV_FP8 || KV == KV_FP8PT || (KV == KV_NVFP4 && HC == 16); }
 constexpr int kBoxDims = 144;                        // dims per TMA box
 constexpr int kBoxBytes = kPage * kBoxDims;          // 9,216
 constexpr int kRawRows = 4 * kBoxBytes;              // 36,864; a per-token-scaled page's scales follow
+constexpr int kNvScaleOff = 2 * kBoxBytes;          // NVFP4: 288 packed bytes per row in two boxes, then
+                                                     // the page's block scales [64][36]
 __host__ __device__ constexpr int rho(int r) { return r ^ ((r >> 2) & 2); }
 // byte offset of the 16-dim chunk c (0..35) of token row t
 __host__ __device__ constexpr int raw_chunk_off(int t, int c) { return (c / 9) * kBoxBytes + t * kBoxDims + (c % 9) * 16; }
@@ -63,10 +68,10 @@ __host__ __device__ constexpr int raw_chunk_off(int t, int c) { return (c / 9) *
 template <int KV>
 constexpr int raw_bytes() {
   return KV == KV_FP8 ? kRawRows
-       : KV == KV_NVFP4 ? kPage * (kPacked + kScales) : KV == KV_FP8PT ? kRawRows + 4 * kPage : 0;
+       : KV == KV_NVFP4 ? kNvScaleOff + kPage * kScales : KV == KV_FP8PT ? kRawRows + 4 * kPage : 0;
 }
-template <int KV>
-constexpr int tile_bytes() { return raw_operands<KV>() ? 0 : kPage * kRowBytes; }
+template <int KV, int HC>
+constexpr int tile_bytes() { return raw_operands<KV, HC>() ? 0 : kPage * kRowBytes; }
 
 constexpr int kNT = 256;                   // threads per CTA: every warp dequantizes
 
@@ -77,19 +82,19 @@ constexpr int pairs() { return (HC / 16) * ((HC / 16) >= 3 ? 1 : 4 / (HC / 16));
 // Logit exchange buffers: 4 KB per warp, two sets (alternate pages) on the raw-operand path, whose
 // warps run without a CTA-wide barrier per page.
 template <int KV, int HC>
-constexpr int xbuf_bytes() { return pairs<HC>() * 8192 * (raw_operands<KV>() ? 2 : 1); }
+constexpr int xbuf_bytes() { return pairs<HC>() * 8192 * (raw_operands<KV, HC>() ? 2 : 1); }
 
 // Raw page buffers: as many as fit up to three (pages fetched that far ahead), at least one.
 template <int KV, int HC>
 constexpr int raw_bufs() {
   return KV == KV_BF16 ? 0
-       : HC * kRowBytes + tile_bytes<KV>() + 3 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 3
-       : HC * kRowBytes + tile_bytes<KV>() + 2 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 2 : 1;
+       : HC * kRowBytes + tile_bytes<KV, HC>() + 3 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 3
+       : HC * kRowBytes + tile_bytes<KV, HC>() + 2 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 2 : 1;
 }
 
 template <int KV, int HC>
 constexpr int smem_bytes() {
-  return HC * kRowBytes + tile_bytes<KV>() + raw_bufs<KV, HC>() * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64;
+  return HC * kRowBytes + tile_bytes<KV, HC>() + raw_bufs<KV, HC>() * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64;
 }
 
 // Raw bytes of one page (FP8, per-token-scaled FP8: the page; NVFP4: data then block scales) into a
@@ -124,9 +129,11 @@ __device__ __forceinline__ void fetch_raw_page(const DecodeArgs& a, const CUtens
     return;
   }
   tc::mbar_arrive_expect_tx(bar, raw_bytes<KV>());
+  constexpr int kBoxes = KV == KV_NVFP4 ? 2 : 4;
 #pragma unroll
-  for (int b = 0; b < 4; ++b) tc::tma_load_3d(s_raw + b * kBoxBytes, map, b * kBoxDims, 0, static_cast<int>(page), bar);
+  for (int b = 0; b < kBoxes; ++b) tc::tma_load_3d(s_raw + b * kBoxBytes, map, b * kBoxDims, 0, static_cast<int>(page), bar);
   if (KV == KV_FP8PT) tc::bulk_load(s_raw + kRawRows, a.kv + page * kPtPageBytes + kPtScaleOff, 4 * kPage, bar);
+  if (KV == KV_NVFP4) tc::bulk_load(s_raw + kNvScaleOff, a.kv_scale + page * (kPage * kScales), kPage * kScales, bar);
 }
 
 // Fetch the raw bytes of one page (or, for BF16, the page itself) with cp.async.
@@ -242,11 +249,11 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
   constexpr int NT = kNT;
   constexpr int NB = raw_bufs<KV, HC>();
   constexpr int NBx = NB > 0 ? NB : 1;
-  constexpr bool RAW = raw_operands<KV>();
+  constexpr bool RAW = raw_operands<KV, HC>();
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_q = smem;
   uint8_t* s_kv = s_q + HC * kRowBytes;      // the dequantized page tile (not on the raw-operand path)
-  uint8_t* s_raw = s_kv + tile_bytes<KV>();
+  uint8_t* s_raw = s_kv + tile_bytes<KV, HC>();
   float* s_x = reinterpret_cast<float*>(s_raw + NB * raw_bytes<KV>());
   uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + NPAIR * 2 * 1024 * (RAW ? 2 : 1));
   // NB FULL barriers, then (raw-operand path) NB EMPTY barriers: 8-byte aligned
@@ -313,7 +320,24 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       if (qm != 0u && qm < 0x7F80u) sh = max(-100, min(113, static_cast<int>(qm >> 7) - 127 - 14));
       const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
       q_scale_log2 = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
-      if constexpr (RAW) {
+      if constexpr (RAW && KV == KV_NVFP4) {
+        // NVFP4 raw-operand path: within every 32 dims (16 dim pairs), pair position i holds pair
+        // 4(i % 4) + i / 4, the order a lane's K fragment bytes come in (a 4 x 4 transpose)
+        for (int c = tid; c < HC * (kLatent / 32); c += NT) {
+          const int row = c / (kLatent / 32), ch = c % (kLatent / 32);
+          uint4* p = reinterpret_cast<uint4*>(s_q + row * kRowBytes + ch * 64);
+          uint32_t w[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 v = p[u];
+            w[4 * u] = v.x; w[4 * u + 1] = v.y; w[4 * u + 2] = v.z; w[4 * u + 3] = v.w;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            p[u] = make_uint4(dev::bf16x2_to_f16x2(w[u], down), dev::bf16x2_to_f16x2(w[4 + u], down),
+                              dev::bf16x2_to_f16x2(w[8 + u], down), dev::bf16x2_to_f16x2(w[12 + u], down));
+        }
+      } else if constexpr (RAW) {
         // raw-operand path: within every 16 dims, position 2a + e holds dim 4a + e and position
         // 8 + 2a + e holds dim 4a + 2 + e (a < 4, e < 2), the order a lane's K fragment bytes come in
         for (int c = tid; c < HC * (kLatent / 16); c += NT) {
@@ -387,12 +411,16 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         // rows past the page's tokens (and their scales) read as zeros: P is 0 there, and V must not
         // bring NaN codes into P.V
         if (live < kPage) {
-          for (int c = tid; c < (kPage - live) * (kLatent / 16); c += NT) {
-            const int t = live + c / (kLatent / 16), ch = c % (kLatent / 16);
+          constexpr int kChunks = KV == KV_NVFP4 ? kPacked / 16 : kLatent / 16;
+          for (int c = tid; c < (kPage - live) * kChunks; c += NT) {
+            const int t = live + c / kChunks, ch = c % kChunks;
             *reinterpret_cast<uint4*>(rbuf + raw_chunk_off(t, ch)) = make_uint4(0, 0, 0, 0);
           }
           if (KV == KV_FP8PT)
             for (int t = live + tid; t < kPage; t += NT) reinterpret_cast<float*>(rbuf + kRawRows)[t] = 0.0f;
+          if (KV == KV_NVFP4)      // block scales too: an unused slot's scale may be the NaN code
+            for (int c = tid; c < (kPage - live) * (kScales / 4); c += NT)
+              reinterpret_cast<uint32_t*>(rbuf + kNvScaleOff + live * kScales)[c] = 0u;
           __syncthreads();
         }
         if (j + 1 < seg.num_pages) page = a.kv_indices[seg.page_begin + j + 1];
@@ -412,7 +440,58 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       float s[2 * NP][4];
 #pragma unroll
       for (int n = 0; n < 2 * NP; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
-      if constexpr (RAW) {
+      if constexpr (RAW && KV == KV_NVFP4) {
+        // NVFP4: a 16-byte chunk c of a row is 32 dims, two 16-element blocks. As for FP8, lane l
+        // addresses row rho(4((l & 7) >> 1) + (l & 1) + 2jj) of tile p, chunk (l >> 3) of a pair; it
+        // receives bytes 4t4 .. 4t4+3 of the row of logit column g8: dims 32c + 8t4 .. +7, all in
+        // block 2c + (t4 >> 1). Bytes 4t4, 4t4+1 form the B fragment of k-step 2c, bytes 4t4+2,
+        // 4t4+3 that of k-step 2c + 1 (Q is stored to match); each code pair times the block scale
+        // in F16 is exact.
+        const int kr = lane & 7;
+        const uint8_t* sc = rbuf + kNvScaleOff;
+        constexpr bool kSplit = NP <= 2;
+        float s2[kSplit ? 2 * NP : 1][4];
+#pragma unroll
+        for (int n = 0; n < (kSplit ? 2 * NP : 1); ++n) s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.0f;
+#pragma unroll
+        for (int cb = 0; cb < 5; ++cb) {       // chunks 2cb, 2cb + 1 of the half's nine (one in the last)
+          constexpr int kChunks = 9;
+          uint32_t aq[4][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (2 * cb + i / 2 < kChunks)
+              dev::ldsm_x4(a_q + q_lane + (half * 288 + 16 * (4 * cb + i)) * 2, aq[i][0], aq[i][1], aq[i][2], aq[i][3]);
+#pragma unroll
+          for (int p = 0; p < NP; ++p)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const uint32_t addr = a_rb + raw_chunk_off(t0 + 16 * p + rho(4 * (kr >> 1) + (kr & 1) + 2 * jj),
+                                                         half * 9 + 2 * cb + (lane >> 3));
+              const int mytok = t0 + 16 * p + rho(4 * (g8 >> 1) + (g8 & 1) + 2 * jj);
+              uint32_t r[2];
+              if (cb < 4) dev::ldsm_x2(addr, r[0], r[1]);
+              else dev::ldsm_x1(addr, r[0]);
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                if (2 * cb + u >= kChunks) continue;
+                const uint32_t sb = sc[mytok * kScales + 2 * (half * 9 + 2 * cb + u) + (t4 >> 1)];
+                const uint32_t sh2 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
+                const uint32_t w = r[u];
+                dev::mma_f16(s[2 * p + jj], aq[2 * u][0], aq[2 * u][1], aq[2 * u][2], aq[2 * u][3],
+                             dev::nvfp4x2_to_f16x2(w & 0xFFu, sh2), dev::nvfp4x2_to_f16x2((w >> 8) & 0xFFu, sh2));
+                dev::mma_f16(kSplit ? s2[kSplit ? 2 * p + jj : 0] : s[2 * p + jj],
+                             aq[2 * u + 1][0], aq[2 * u + 1][1], aq[2 * u + 1][2], aq[2 * u + 1][3],
+                             dev::nvfp4x2_to_f16x2((w >> 16) & 0xFFu, sh2), dev::nvfp4x2_to_f16x2(w >> 24, sh2));
+              }
+            }
+        }
+        if constexpr (kSplit) {
+#pragma unroll
+          for (int n = 0; n < 2 * NP; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[n][i] += s2[n][i];
+        }
+      } else if constexpr (RAW) {
         // K fragments straight from the page bytes: per 16-token tile p and n8 tile jj, lane l
         // addresses tile row rho(4((l & 7) >> 1) + (l & 1) + 2jj), k-step (l >> 3) of a block of
         // four; it receives dims 4t4 .. 4t4+3 of the row of logit column g8, i.e. B[2t4, 2t4+1] and
@@ -542,7 +621,43 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         const uint32_t pa1 = dev::pack_f16x2(s[2 * kt][2] * sa[0], s[2 * kt][3] * sa[1]);
         const uint32_t pa2 = dev::pack_f16x2(s[2 * kt + 1][0] * sb[0], s[2 * kt + 1][1] * sb[1]);
         const uint32_t pa3 = dev::pack_f16x2(s[2 * kt + 1][2] * sb[0], s[2 * kt + 1][3] * sb[1]);
-        if constexpr (RAW) {
+        if constexpr (RAW && KV == KV_NVFP4) {
+          // NVFP4 V fragments: the transposing byte ldmatrix gives lane l, per 16-byte chunk (32
+          // dims), tile rows 4t4 .. 4t4+3 of byte column g8 (dims 2g8, 2g8 + 1: low and high
+          // nibbles) and of byte column 8 + g8 (dims 16 + 2g8, 17 + 2g8). Nibble shuffles pair
+          // the four tokens' codes per dim; each code pair times its two tokens' block scales in
+          // F16 is exact. Output tiles come per dim parity: o[4c] holds dims 32c + 2n, o[4c + 1]
+          // dims 32c + 2n + 1, o[4c + 2] and o[4c + 3] the same 16 dims higher (c = chunk of the
+          // warp's 256 dims); the epilogue writes them back in order.
+          const int vt = t0 + kt * 16 + rho(lane & 15);
+          const uint8_t* sc = rbuf + kNvScaleOff;
+          int stok[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) stok[u] = t0 + kt * 16 + rho(4 * t4 + u);
+#pragma unroll
+          for (int vq = 0; vq < 4; ++vq) {        // chunks 2vq, 2vq + 1 of the warp's eight
+            uint32_t r[4];
+            dev::ldsm_t8_x2(a_rb + raw_chunk_off(vt, half * 8 + 2 * vq + (lane >> 4)), r[0], r[1], r[2], r[3]);
+            // the four tokens' scales of blocks 2c .. 2c + 3 (c = the pair's first chunk in the row)
+            const int blk0 = 2 * (half * 8 + 2 * vq);
+            uint32_t sw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sw[u] = *reinterpret_cast<const uint32_t*>(sc + stok[u] * kScales + blk0);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {          // r[m]: chunk 2vq + m / 2, dims +16 * (m & 1)
+              const int b = m;                       // block 2c + m within the four loaded
+              const uint32_t s01 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(sw[0], sw[1], b | ((4 + b) << 4))));
+              const uint32_t s23 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(sw[2], sw[3], b | ((4 + b) << 4))));
+              const uint32_t x = r[m];
+              const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+              const uint32_t e01 = (lo & 0xFu) | ((lo >> 4) & 0xF0u), e23 = ((lo >> 16) & 0xFu) | ((lo >> 20) & 0xF0u);
+              const uint32_t o01 = (hi & 0xFu) | ((hi >> 4) & 0xF0u), o23 = ((hi >> 16) & 0xFu) | ((hi >> 20) & 0xF0u);
+              const int nt = 4 * (2 * vq + (m >> 1)) + 2 * (m & 1);
+              dev::mma_f16(o[nt], pa0, pa1, pa2, pa3, dev::nvfp4x2_to_f16x2(e01, s01), dev::nvfp4x2_to_f16x2(e23, s23));
+              dev::mma_f16(o[nt + 1], pa0, pa1, pa2, pa3, dev::nvfp4x2_to_f16x2(o01, s01), dev::nvfp4x2_to_f16x2(o23, s23));
+            }
+          }
+        } else if constexpr (RAW) {
           // V fragments straight from the page bytes: lanes 0..15 address the tile's 16 rows (token
           // rho(r) for row r) at a 16-dim block, lanes 16..31 at the next block; each lane receives
           // rows 4t4 .. 4t4+3 (P's k order above) of dims g8 and 8 + g8 of each block
@@ -592,7 +707,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       // (O, m, l) in their fragment order, the tg = 0 pair of the same heads reads them back
       float* mrg = reinterpret_cast<float*>(s_kv);
       constexpr int kSlot = 32 * 128 + 32 * 4;            // one warp's O fragments, then m and l
-      static_assert(NG * (TG - 1) * 2 * kSlot * 4 <= tile_bytes<KV>() + NB * raw_bytes<KV>() + NPAIR * 8192,
+      static_assert(NG * (TG - 1) * 2 * kSlot * 4 <= tile_bytes<KV, HC>() + NB * raw_bytes<KV>() + xbuf_bytes<KV, HC>(),
                     "merge slots fit in the page tile, raw buffers and exchange buffers");
       auto slot = [&](int g, int t, int hf) { return mrg + ((g * (TG - 1) + (t - 1)) * 2 + hf) * kSlot; };
       if (tg > 0) {
@@ -637,29 +752,54 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int head = h0 + grp * 16 + g8 + 8 * r;
+      // output dim of element e (0..3) of a lane's four consecutive dims 4t4 + e: NVFP4 tiles hold
+      // even / odd dims apart (o[4c + 2h + (e & 1)][2r + (e >> 1)] for dims 32c + 16h + 4t4 + e),
+      // the other pools consecutive pairs (o[q][2r + (e & 1)] for dims 8q + 2t4 + e)
       if (seg.partial < 0) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + (static_cast<int64_t>(seg.req) * a.heads + head) * kDv + half * 256);
+        uint16_t* dst = a.out + (static_cast<int64_t>(seg.req) * a.heads + head) * kDv + half * 256;
         const float sc = inv[r] * a.out_scale;
+        if constexpr (RAW && KV == KV_NVFP4) {
 #pragma unroll
-        for (int nt = 0; nt < 32; ++nt) dst[(nt * 8 + 2 * t4) / 2] = dev::pack_bf16x2(o[nt][2 * r] * sc, o[nt][2 * r + 1] * sc);
+          for (int q = 0; q < 16; ++q) {         // 16-dim groups: chunk q / 2, half q & 1
+            const int nt = 4 * (q >> 1) + 2 * (q & 1);
+            *reinterpret_cast<uint2*>(dst + 16 * q + 4 * t4) =
+                make_uint2(dev::pack_bf16x2(o[nt][2 * r] * sc, o[nt + 1][2 * r] * sc),
+                           dev::pack_bf16x2(o[nt][2 * r + 1] * sc, o[nt + 1][2 * r + 1] * sc));
+          }
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < 32; ++nt)
+            reinterpret_cast<uint32_t*>(dst)[(nt * 8 + 2 * t4) / 2] = dev::pack_bf16x2(o[nt][2 * r] * sc, o[nt][2 * r + 1] * sc);
+        }
         if (half == 0 && t4 == 0 && a.lse) a.lse[static_cast<int64_t>(seg.req) * a.heads + head] = lse2[r] * 0.69314718055994531f;
       } else {
-        float2* dst = reinterpret_cast<float2*>(a.part_o + (static_cast<int64_t>(seg.partial) * a.heads + head) * kDv + half * 256);
+        float* dst = a.part_o + (static_cast<int64_t>(seg.partial) * a.heads + head) * kDv + half * 256;
+        if constexpr (RAW && KV == KV_NVFP4) {
 #pragma unroll
-        for (int nt = 0; nt < 32; ++nt) dst[(nt * 8 + 2 * t4) / 2] = make_float2(o[nt][2 * r] * inv[r], o[nt][2 * r + 1] * inv[r]);
+          for (int q = 0; q < 16; ++q) {
+            const int nt = 4 * (q >> 1) + 2 * (q & 1);
+            *reinterpret_cast<float4*>(dst + 16 * q + 4 * t4) =
+                make_float4(o[nt][2 * r] * inv[r], o[nt + 1][2 * r] * inv[r], o[nt][2 * r + 1] * inv[r], o[nt + 1][2 * r + 1] * inv[r]);
+          }
+        } else {
+#pragma unroll
+          for (int nt = 0; nt < 32; ++nt)
+            reinterpret_cast<float2*>(dst)[(nt * 8 + 2 * t4) / 2] = make_float2(o[nt][2 * r] * inv[r], o[nt][2 * r + 1] * inv[r]);
+        }
         if (half == 0 && t4 == 0) a.part_lse[static_cast<int64_t>(seg.partial) * a.heads + head] = lse2[r];
       }
     }
   }
 }
 
-// The pool as a 3-D tensor of bytes {576 dims, 64 tokens, pages} (page stride 36,864 or 37,120) for
-// the raw-operand path's TMA loads: box {144, 64, 1}, no swizzle, no interleave.
+// The pool as a 3-D tensor of bytes {row bytes, 64 tokens, pages} (576 per row and a page stride of
+// 36,864 or 37,120 for the FP8 pools, 288 and 18,432 for NVFP4 codes) for the raw-operand path's TMA
+// loads: box {144, 64, 1}, no swizzle, no interleave.
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-cudaError_t encode_kv_map(const DecodeArgs& a, int64_t page_bytes, CUtensorMap* map) {
+cudaError_t encode_kv_map(const DecodeArgs& a, int64_t row_bytes, int64_t page_bytes, CUtensorMap* map) {
   static EncodeTiledFn fn = nullptr;
   if (fn == nullptr) {
     void* p = nullptr;
@@ -669,9 +809,9 @@ cudaError_t encode_kv_map(const DecodeArgs& a, int64_t page_bytes, CUtensorMap* 
       return cudaErrorNotSupported;
     fn = reinterpret_cast<EncodeTiledFn>(p);
   }
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kLatent), static_cast<cuuint64_t>(kPage),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(kPage),
                               static_cast<cuuint64_t>(a.num_pages)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kLatent), static_cast<cuuint64_t>(page_bytes)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(page_bytes)};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBoxDims), static_cast<cuuint32_t>(kPage), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(a.kv), dims, strides, box, estr,
@@ -691,8 +831,9 @@ cudaError_t launch_kv_hc(const DecodeArgs& a, cudaStream_t s) {
   }
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
-  if (raw_operands<KV>() && a.num_pages > 0) {
-    const cudaError_t e = encode_kv_map(a, KV == KV_FP8PT ? kPtPageBytes : kPage * kLatent, &map);
+  if (raw_operands<KV, HC>() && a.num_pages > 0) {
+    const cudaError_t e = KV == KV_NVFP4 ? encode_kv_map(a, kPacked, kPage * kPacked, &map)
+                        : encode_kv_map(a, kLatent, KV == KV_FP8PT ? kPtPageBytes : kPage * kLatent, &map);
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = static_cast<unsigned>(a.num_workers * a.ctas_per_worker);
