@@ -57,11 +57,13 @@ def peaks():
     return p
 
 
-def kernel_source_digest():
+def kernel_source_digest(tu: str = "decode_tc.cu"):
+    """Digest of the sources the timed decode kernel is compiled from: its translation unit and the
+    library headers (a change elsewhere in the library does not change this kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_kv_paged_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f == tu or f.endswith((".cuh", ".h")):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     return h.hexdigest()[:16]
@@ -407,6 +409,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--algo", type=int, default=0)
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--heads", type=int, default=128,
+                    help="query heads of the timed workload (128 is the headline; fewer for profiling the few-heads path)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
     args = ap.parse_args()
@@ -428,6 +432,8 @@ def main():
 
     # ---- headline: FP8, 44 x 32K, 128 heads ----
     w = synth.workload(MAIN, device=dev)
+    if args.heads != 128:
+        w = with_heads(w, args.heads)
     pb = Problem(q, w, q.KV_FP8_E4M3, algo=args.algo)
     torch.cuda.empty_cache()          # drop the generator's temporaries before timing / profiling
     with ClockSampler(local) as clk:
