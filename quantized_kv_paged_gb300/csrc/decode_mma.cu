@@ -79,17 +79,32 @@ constexpr int kNT = 256;                   // threads per CTA: every warp dequan
 template <int HC>
 constexpr int pairs() { return (HC / 16) * ((HC / 16) >= 3 ? 1 : 4 / (HC / 16)); }
 
-// Logit exchange buffers: 4 KB per warp, two sets (alternate pages) on the raw-operand path, whose
-// warps run without a CTA-wide barrier per page.
+// Token groups per CTA (16 heads: 4 of 16 tokens; 32: 2 of 32; 48 and 64: 1 of 64) and pages per
+// iteration: on the raw-operand path with 16 heads each warp takes its 16 tokens of two pages at once
+// (twice the independent MMA chains per warp, half the per-page barriers and exchanges).
+template <int HC>
+constexpr int token_groups() { return (HC / 16) >= 3 ? 1 : 4 / (HC / 16); }
 template <int KV, int HC>
-constexpr int xbuf_bytes() { return pairs<HC>() * 8192 * (raw_operands<KV, HC>() ? 2 : 1); }
+constexpr int pages_per_iter() { return raw_operands<KV, HC>() && token_groups<HC>() == 4 ? 2 : 1; }
+// Logit exchange buffer of one warp: its partial logits (2 n8 tiles x 4 x 32 floats per 16-token
+// tile); two sets (alternate iterations) on the raw-operand path, whose warps run without a CTA-wide
+// barrier per page.
+template <int KV, int HC>
+constexpr int xfloats() {
+  // the tile path keeps 1024 floats per warp: its merge slots at segment end reuse this space
+  return raw_operands<KV, HC>() ? 256 * (kPage / token_groups<HC>() / 16) * pages_per_iter<KV, HC>() : 1024;
+}
+template <int KV, int HC>
+constexpr int xbuf_bytes() { return pairs<HC>() * 2 * xfloats<KV, HC>() * 4 * (raw_operands<KV, HC>() ? 2 : 1); }
 
-// Raw page buffers: as many as fit up to three (pages fetched that far ahead), at least one.
+// Raw page buffers: as many as fit up to four (pages fetched that far ahead), at least one.
+template <int KV, int HC>
+constexpr int raw_bufs_fit(int nb) {
+  return HC * kRowBytes + tile_bytes<KV, HC>() + nb * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024;
+}
 template <int KV, int HC>
 constexpr int raw_bufs() {
-  return KV == KV_BF16 ? 0
-       : HC * kRowBytes + tile_bytes<KV, HC>() + 3 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 3
-       : HC * kRowBytes + tile_bytes<KV, HC>() + 2 * raw_bytes<KV>() + xbuf_bytes<KV, HC>() + 64 <= 232448 - 1024 ? 2 : 1;
+  return KV == KV_BF16 ? 0 : raw_bufs_fit<KV, HC>(4) ? 4 : raw_bufs_fit<KV, HC>(3) ? 3 : raw_bufs_fit<KV, HC>(2) ? 2 : 1;
 }
 
 template <int KV, int HC>
@@ -242,7 +257,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
   // With few heads the page's 64 tokens are split among warp pairs too, so that all 8 warps do
   // math: TG token groups of TPG tokens, each pair with its own softmax state, merged at the end
   // of a segment. 16 heads: 4 x 16 tokens; 32: 2 x 32; 48 and 64: 1 x 64.
-  constexpr int TG = NG >= 3 ? 1 : 4 / NG;
+  constexpr int TG = token_groups<HC>();
   constexpr int NPAIR = NG * TG;
   constexpr int TPG = kPage / TG;
   constexpr int NP = TPG / 16;      // 16-token tiles per token group
@@ -250,12 +265,17 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
   constexpr int NB = raw_bufs<KV, HC>();
   constexpr int NBx = NB > 0 ? NB : 1;
   constexpr bool RAW = raw_operands<KV, HC>();
+  constexpr int PPI = pages_per_iter<KV, HC>();   // pages per iteration
+  constexpr int NPI = NP * PPI;                   // 16-token tiles per warp per iteration
+  constexpr int XF = xfloats<KV, HC>();
+  static_assert(2 * NPI * 4 * 32 <= XF, "exchange buffer");
+  static_assert(PPI == 1 || NB >= 2 * PPI, "two pages in flight ahead of the pair in use");
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* s_q = smem;
   uint8_t* s_kv = s_q + HC * kRowBytes;      // the dequantized page tile (not on the raw-operand path)
   uint8_t* s_raw = s_kv + tile_bytes<KV, HC>();
   float* s_x = reinterpret_cast<float*>(s_raw + NB * raw_bytes<KV>());
-  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + NPAIR * 2 * 1024 * (RAW ? 2 : 1));
+  uint32_t* s_qmax = reinterpret_cast<uint32_t*>(s_x + NPAIR * 2 * XF * (RAW ? 2 : 1));
   // NB FULL barriers, then (raw-operand path) NB EMPTY barriers: 8-byte aligned
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_qmax + 2);
   const uint32_t a_q = dev::smem_u32(s_q), a_kv = dev::smem_u32(s_kv), a_raw = dev::smem_u32(s_raw);
@@ -284,8 +304,8 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
   const uint32_t q_lane = ((grp * 16 + (lane & 15)) * kRow + (lane >> 4) * 8) * 2;
   const uint32_t k_lane = (((lane & 7) + ((lane >> 4) << 3)) * kRow + ((lane >> 3) & 1) * 8) * 2;
   const uint32_t v_lane = (((lane & 7) + ((lane >> 3) & 1) * 8) * kRow + half * 256 + (lane >> 4) * 8) * 2;
-  float* const x_mine0 = s_x + (pi * 2 + half) * 1024;
-  float* const x_peer0 = s_x + (pi * 2 + (half ^ 1)) * 1024;
+  float* const x_mine0 = s_x + (pi * 2 + half) * XF;
+  float* const x_peer0 = s_x + (pi * 2 + (half ^ 1)) * XF;
 
   int cur_req = -1;
   float q_scale_log2 = a.scale_log2;
@@ -377,53 +397,89 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         fetch_page<KV>(a, a.kv_indices[seg.page_begin + k], a_raw + k * raw_bytes<KV>(), a_bar + 8 * k);
     }
     int64_t page = a.kv_indices[seg.page_begin];
-    for (int j = 0; j < seg.num_pages; ++j) {
-      const int valid = min(kPage, seg.num_tokens - j * kPage);
-      const bool page_ok = page >= 0 && page < a.num_pages;
-      const int buf = NB > 0 ? j % NB : 0;
-      if (RAW && tid == 0 && j >= 1 && j - 1 + NB < seg.num_pages) {
-        // the buffer of page j - 1 takes page j - 1 + NB once every warp is done with page j - 1
-        // (its fills[]-th use: EMPTY completes once per use)
-        const int pb = (j - 1) % NB;
-        if (!tc::mbar_wait(a_bar + 8 * (NB + pb), (fills[pb] - 1) & 1)) atomicOr(a.status, 16);
-        tc::fence_proxy_async_smem();
-        fetch_raw_page<KV>(a, &kv_map, a.kv_indices[seg.page_begin + j - 1 + NB], a_raw + pb * raw_bytes<KV>(),
-                           a_bar + 8 * pb);
-      }
-      if (KV == KV_BF16) {
-        issue_page<KV, NT>(a, page, valid, a_raw, a_kv, tid);
-        dev::cp_async_wait_all();
-      } else {
-        // bounded wait: a timeout sets a status bit, and the page then reads as whatever is there
-        if (!tc::mbar_wait(a_bar + 8 * buf, fills[buf] & 1)) {
-          if (lane == 0) atomicOr(a.status, 16);
-        }
-        ++fills[buf];
-      }
-      const int live = page_ok ? valid : 0;
-      uint8_t* rbuf = s_raw + buf * raw_bytes<KV>();
-      const uint32_t a_rb = a_raw + buf * raw_bytes<KV>();
-      // logit exchange buffers of this page (two sets on the raw-operand path: a warp may write page
-      // j + 1's while its peer still reads page j's; page j + 2 waits for the pair barrier of j + 1)
-      float* x_mine = x_mine0 + (RAW && (j & 1) ? NPAIR * 2 * 1024 : 0);
-      float* x_peer = x_peer0 + (RAW && (j & 1) ? NPAIR * 2 * 1024 : 0);
-      if constexpr (RAW) {
-        // rows past the page's tokens (and their scales) read as zeros: P is 0 there, and V must not
-        // bring NaN codes into P.V
-        if (live < kPage) {
-          constexpr int kChunks = KV == KV_NVFP4 ? kPacked / 16 : kLatent / 16;
-          for (int c = tid; c < (kPage - live) * kChunks; c += NT) {
-            const int t = live + c / kChunks, ch = c % kChunks;
-            *reinterpret_cast<uint4*>(rbuf + raw_chunk_off(t, ch)) = make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < seg.num_pages; j += PPI) {
+      if (RAW && tid == 0 && j >= PPI) {
+        // the buffers of the previous iteration's pages take the pages NB further on once every warp
+        // is done with them (each buffer's fills[]-th use: EMPTY completes once per use)
+#pragma unroll
+        for (int u = 0; u < PPI; ++u) {
+          const int pp = j - PPI + u;
+          if (pp + NB < seg.num_pages) {
+            const int pb = pp % NB;
+            if (!tc::mbar_wait(a_bar + 8 * (NB + pb), (fills[pb] - 1) & 1)) atomicOr(a.status, 16);
+            tc::fence_proxy_async_smem();
+            fetch_raw_page<KV>(a, &kv_map, a.kv_indices[seg.page_begin + pp + NB], a_raw + pb * raw_bytes<KV>(),
+                               a_bar + 8 * pb);
           }
-          if (KV == KV_FP8PT)
-            for (int t = live + tid; t < kPage; t += NT) reinterpret_cast<float*>(rbuf + kRawRows)[t] = 0.0f;
-          if (KV == KV_NVFP4)      // block scales too: an unused slot's scale may be the NaN code
-            for (int c = tid; c < (kPage - live) * (kScales / 4); c += NT)
-              reinterpret_cast<uint32_t*>(rbuf + kNvScaleOff + live * kScales)[c] = 0u;
+        }
+      }
+      // this iteration's pages: buffer, valid tokens (0 past the segment: such a tile reads page j's
+      // buffer and is masked whole)
+      int live_u[PPI], buf_u[PPI];
+      uint32_t rb_u[PPI];
+      uint8_t* rbuf_u[PPI];
+      bool any_partial = false;
+#pragma unroll
+      for (int u = 0; u < PPI; ++u) {
+        const int jp = j + u;
+        const bool has = jp < seg.num_pages;
+        const int64_t pg_u = u == 0 ? page : (has ? static_cast<int64_t>(a.kv_indices[seg.page_begin + jp]) : -1);
+        const int valid_u = has ? min(kPage, seg.num_tokens - jp * kPage) : 0;
+        buf_u[u] = NB > 0 ? (has ? jp : j) % NB : 0;
+        if (has) {
+          if (KV == KV_BF16) {
+            issue_page<KV, NT>(a, pg_u, valid_u, a_raw, a_kv, tid);
+            dev::cp_async_wait_all();
+          } else {
+            // bounded wait: a timeout sets a status bit, and the page then reads as whatever is there
+            if (!tc::mbar_wait(a_bar + 8 * buf_u[u], fills[buf_u[u]] & 1)) {
+              if (lane == 0) atomicOr(a.status, 16);
+            }
+            ++fills[buf_u[u]];
+          }
+        }
+        live_u[u] = (pg_u >= 0 && pg_u < a.num_pages) ? valid_u : 0;
+        rb_u[u] = a_raw + buf_u[u] * raw_bytes<KV>();
+        rbuf_u[u] = s_raw + buf_u[u] * raw_bytes<KV>();
+        any_partial |= has && live_u[u] < kPage;
+      }
+      const int live = live_u[0];
+      const int buf = buf_u[0];
+      uint8_t* rbuf = rbuf_u[0];
+      const uint32_t a_rb = rb_u[0];
+      // tile p of this iteration: page j + p / NP, tokens t0 + 16 (p % NP) of it
+      auto tt0 = [&](int p) { return t0 + 16 * (p % NP); };
+      auto trb = [&](int p) { return rb_u[p / NP]; };
+      auto trbuf = [&](int p) { return rbuf_u[p / NP]; };
+      auto tlive = [&](int p) { return live_u[p / NP]; };
+      // logit exchange buffers of this iteration (two sets on the raw-operand path: a warp may write
+      // iteration i + 1's while its peer still reads iteration i's; i + 2 waits for the pair barrier of
+      // i + 1)
+      float* x_mine = x_mine0 + (RAW && ((j / PPI) & 1) ? NPAIR * 2 * XF : 0);
+      float* x_peer = x_peer0 + (RAW && ((j / PPI) & 1) ? NPAIR * 2 * XF : 0);
+      if constexpr (RAW) {
+        // rows past a page's tokens (and their scales) read as zeros: P is 0 there, and V must not
+        // bring NaN codes into P.V
+        if (any_partial) {
+#pragma unroll
+          for (int u = 0; u < PPI; ++u) {
+            if (j + u >= seg.num_pages || live_u[u] >= kPage) continue;
+            uint8_t* rb = rbuf_u[u];
+            const int lv = live_u[u];
+            constexpr int kChunks = KV == KV_NVFP4 ? kPacked / 16 : kLatent / 16;
+            for (int c = tid; c < (kPage - lv) * kChunks; c += NT) {
+              const int t = lv + c / kChunks, ch = c % kChunks;
+              *reinterpret_cast<uint4*>(rb + raw_chunk_off(t, ch)) = make_uint4(0, 0, 0, 0);
+            }
+            if (KV == KV_FP8PT)
+              for (int t = lv + tid; t < kPage; t += NT) reinterpret_cast<float*>(rb + kRawRows)[t] = 0.0f;
+            if (KV == KV_NVFP4)      // block scales too: an unused slot's scale may be the NaN code
+              for (int c = tid; c < (kPage - lv) * (kScales / 4); c += NT)
+                reinterpret_cast<uint32_t*>(rb + kNvScaleOff + lv * kScales)[c] = 0u;
+          }
           __syncthreads();
         }
-        if (j + 1 < seg.num_pages) page = a.kv_indices[seg.page_begin + j + 1];
+        if (j + PPI < seg.num_pages) page = a.kv_indices[seg.page_begin + j + PPI];
       } else {
         __syncthreads();
         dequant_page<KV, NT>(rbuf, s_kv, live, tid);
@@ -437,9 +493,9 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       if (mma_warp) {
 
       // ---- S partial = Q[:, my dims] K[my tokens, my dims]^T  (16 heads x TPG tokens) ----
-      float s[2 * NP][4];
+      float s[2 * NPI][4];
 #pragma unroll
-      for (int n = 0; n < 2 * NP; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
+      for (int n = 0; n < 2 * NPI; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
       if constexpr (RAW && KV == KV_NVFP4) {
         // NVFP4: a 16-byte chunk c of a row is 32 dims, two 16-element blocks. As for FP8, lane l
         // addresses row rho(4((l & 7) >> 1) + (l & 1) + 2jj) of tile p, chunk (l >> 3) of a pair; it
@@ -448,11 +504,10 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         // 4t4+3 that of k-step 2c + 1 (Q is stored to match); each code pair times the block scale
         // in F16 is exact.
         const int kr = lane & 7;
-        const uint8_t* sc = rbuf + kNvScaleOff;
-        constexpr bool kSplit = NP <= 2;
-        float s2[kSplit ? 2 * NP : 1][4];
+        constexpr bool kSplit = NPI <= 2;
+        float s2[kSplit ? 2 * NPI : 1][4];
 #pragma unroll
-        for (int n = 0; n < (kSplit ? 2 * NP : 1); ++n) s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.0f;
+        for (int n = 0; n < (kSplit ? 2 * NPI : 1); ++n) s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.0f;
 #pragma unroll
         for (int cb = 0; cb < 5; ++cb) {       // chunks 2cb, 2cb + 1 of the half's nine (one in the last)
           constexpr int kChunks = 9;
@@ -462,12 +517,13 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
             if (2 * cb + i / 2 < kChunks)
               dev::ldsm_x4(a_q + q_lane + (half * 288 + 16 * (4 * cb + i)) * 2, aq[i][0], aq[i][1], aq[i][2], aq[i][3]);
 #pragma unroll
-          for (int p = 0; p < NP; ++p)
+          for (int p = 0; p < NPI; ++p)
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
-              const uint32_t addr = a_rb + raw_chunk_off(t0 + 16 * p + rho(4 * (kr >> 1) + (kr & 1) + 2 * jj),
-                                                         half * 9 + 2 * cb + (lane >> 3));
-              const int mytok = t0 + 16 * p + rho(4 * (g8 >> 1) + (g8 & 1) + 2 * jj);
+              const uint32_t addr = trb(p) + raw_chunk_off(tt0(p) + rho(4 * (kr >> 1) + (kr & 1) + 2 * jj),
+                                                           half * 9 + 2 * cb + (lane >> 3));
+              const int mytok = tt0(p) + rho(4 * (g8 >> 1) + (g8 & 1) + 2 * jj);
+              const uint8_t* sc = trbuf(p) + kNvScaleOff;
               uint32_t r[2];
               if (cb < 4) dev::ldsm_x2(addr, r[0], r[1]);
               else dev::ldsm_x1(addr, r[0]);
@@ -487,7 +543,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         }
         if constexpr (kSplit) {
 #pragma unroll
-          for (int n = 0; n < 2 * NP; ++n)
+          for (int n = 0; n < 2 * NPI; ++n)
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[n][i] += s2[n][i];
         }
@@ -499,10 +555,10 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         const int kr = lane & 7;
         // with one or two 16-token tiles, odd k-steps accumulate apart: twice the independent
         // chains of dependent MMAs (four tiles have enough already)
-        constexpr bool kSplit = NP <= 2;
-        float s2[kSplit ? 2 * NP : 1][4];
+        constexpr bool kSplit = NPI <= 2;
+        float s2[kSplit ? 2 * NPI : 1][4];
 #pragma unroll
-        for (int n = 0; n < (kSplit ? 2 * NP : 1); ++n) s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.0f;
+        for (int n = 0; n < (kSplit ? 2 * NPI : 1); ++n) s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.0f;
 #pragma unroll
         for (int kb = 0; kb < 5; ++kb) {       // k-steps 4kb .. 4kb + 3 (two in the last block)
           constexpr int kSteps = 18;
@@ -512,11 +568,11 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
             if (4 * kb + i < kSteps)
               dev::ldsm_x4(a_q + q_lane + (half * 288 + 16 * (4 * kb + i)) * 2, aq[i][0], aq[i][1], aq[i][2], aq[i][3]);
 #pragma unroll
-          for (int p = 0; p < NP; ++p)
+          for (int p = 0; p < NPI; ++p)
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
-              const uint32_t addr = a_rb + raw_chunk_off(t0 + 16 * p + rho(4 * (kr >> 1) + (kr & 1) + 2 * jj),
-                                                         half * 18 + 4 * kb + (lane >> 3));
+              const uint32_t addr = trb(p) + raw_chunk_off(tt0(p) + rho(4 * (kr >> 1) + (kr & 1) + 2 * jj),
+                                                           half * 18 + 4 * kb + (lane >> 3));
               uint32_t r[4];
               if (kb < 4) dev::ldsm_x4(addr, r[0], r[1], r[2], r[3]);
               else dev::ldsm_x2(addr, r[0], r[1]);
@@ -530,7 +586,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         }
         if constexpr (kSplit) {
 #pragma unroll
-          for (int n = 0; n < 2 * NP; ++n)
+          for (int n = 0; n < 2 * NPI; ++n)
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[n][i] += s2[n][i];
         }
@@ -541,7 +597,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         uint32_t a0, a1, a2, a3;
         dev::ldsm_x4(a_q + q_lane + kk * 2, a0, a1, a2, a3);
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
+        for (int p = 0; p < NPI; ++p) {
           uint32_t b0, b1, b2, b3;
           dev::ldsm_x4(a_kv + k_lane + ((t0 + p * 16) * kRow + kk) * 2, b0, b1, b2, b3);
           dev::mma_f16(s[2 * p], a0, a1, a2, a3, b0, b1);
@@ -551,12 +607,12 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       }
       // ---- exchange the partial logits with the peer warp; sum in a fixed order ----
 #pragma unroll
-      for (int n = 0; n < 2 * NP; ++n)
+      for (int n = 0; n < 2 * NPI; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) x_mine[(n * 4 + i) * 32 + lane] = s[n][i];
       dev::named_bar_sync(1 + pi, 64);
 #pragma unroll
-      for (int n = 0; n < 2 * NP; ++n)
+      for (int n = 0; n < 2 * NPI; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float peer = x_peer[(n * 4 + i) * 32 + lane];
@@ -567,24 +623,24 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       // page token of logit column 2t4 + e of n8 tile n: on the raw-operand path tile 2p + jj holds
       // tile rows {0,1,4,5,8,9,12,13} + 2jj (the order the P.V B fragments take them in), through rho
       auto tok_of = [&](int n, int e) {
-        return RAW ? t0 + 16 * (n >> 1) + rho(4 * t4 + e + 2 * (n & 1)) : t0 + n * 8 + 2 * t4 + e;
+        return RAW ? tt0(n >> 1) + rho(4 * t4 + e + 2 * (n & 1)) : t0 + n * 8 + 2 * t4 + e;
       };
-      float sig[2 * NP][2];
+      float sig[2 * NPI][2];
 #pragma unroll
-      for (int n = 0; n < 2 * NP; ++n)
+      for (int n = 0; n < 2 * NPI; ++n)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
           sig[n][e] = KV != KV_FP8PT ? 1.0f
-              : RAW ? reinterpret_cast<const float*>(rbuf + kRawRows)[tok_of(n, e)]
+              : RAW ? reinterpret_cast<const float*>(trbuf(n >> 1) + kRawRows)[tok_of(n, e)]
                     : *reinterpret_cast<const float*>(s_kv + tok_of(n, e) * kRowBytes + kSigByte);
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int n = 0; n < 2 * NP; ++n)
+      for (int n = 0; n < 2 * NPI; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tok = tok_of(n, i & 1);
           const float x = KV == KV_FP8PT ? s[n][i] * sig[n][i & 1] : s[n][i];
-          const float v = tok < live ? x * q_scale_log2 : -INFINITY;
+          const float v = tok < (RAW ? tlive(n >> 1) : live) ? x * q_scale_log2 : -INFINITY;
           s[n][i] = v;
           mx[i >> 1] = fmaxf(mx[i >> 1], v);
         }
@@ -600,7 +656,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         l_r[r] *= alpha[r];
       }
 #pragma unroll
-      for (int n = 0; n < 2 * NP; ++n)
+      for (int n = 0; n < 2 * NPI; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float p = dev::fast_exp2(s[n][i] - mref[i >> 1]);
@@ -614,7 +670,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       }
       // ---- O[:, my 256 dims] += P V ----
 #pragma unroll
-      for (int kt = 0; kt < NP; ++kt) {
+      for (int kt = 0; kt < NPI; ++kt) {
         const float* sa = sig[2 * kt];
         const float* sb = sig[2 * kt + 1];
         const uint32_t pa0 = dev::pack_f16x2(s[2 * kt][0] * sa[0], s[2 * kt][1] * sa[1]);
@@ -629,15 +685,15 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
           // F16 is exact. Output tiles come per dim parity: o[4c] holds dims 32c + 2n, o[4c + 1]
           // dims 32c + 2n + 1, o[4c + 2] and o[4c + 3] the same 16 dims higher (c = chunk of the
           // warp's 256 dims); the epilogue writes them back in order.
-          const int vt = t0 + kt * 16 + rho(lane & 15);
-          const uint8_t* sc = rbuf + kNvScaleOff;
+          const int vt = tt0(kt) + rho(lane & 15);
+          const uint8_t* sc = trbuf(kt) + kNvScaleOff;
           int stok[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) stok[u] = t0 + kt * 16 + rho(4 * t4 + u);
+          for (int u = 0; u < 4; ++u) stok[u] = tt0(kt) + rho(4 * t4 + u);
 #pragma unroll
           for (int vq = 0; vq < 4; ++vq) {        // chunks 2vq, 2vq + 1 of the warp's eight
             uint32_t r[4];
-            dev::ldsm_t8_x2(a_rb + raw_chunk_off(vt, half * 8 + 2 * vq + (lane >> 4)), r[0], r[1], r[2], r[3]);
+            dev::ldsm_t8_x2(trb(kt) + raw_chunk_off(vt, half * 8 + 2 * vq + (lane >> 4)), r[0], r[1], r[2], r[3]);
             // the four tokens' scales of blocks 2c .. 2c + 3 (c = the pair's first chunk in the row)
             const int blk0 = 2 * (half * 8 + 2 * vq);
             uint32_t sw[4];
@@ -661,11 +717,11 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
           // V fragments straight from the page bytes: lanes 0..15 address the tile's 16 rows (token
           // rho(r) for row r) at a 16-dim block, lanes 16..31 at the next block; each lane receives
           // rows 4t4 .. 4t4+3 (P's k order above) of dims g8 and 8 + g8 of each block
-          const int vt = t0 + kt * 16 + rho(lane & 15);
+          const int vt = tt0(kt) + rho(lane & 15);
 #pragma unroll
           for (int vq = 0; vq < 8; ++vq) {
             uint32_t r[4];
-            dev::ldsm_t8_x2(a_rb + raw_chunk_off(vt, half * 16 + 2 * vq + (lane >> 4)), r[0], r[1], r[2], r[3]);
+            dev::ldsm_t8_x2(trb(kt) + raw_chunk_off(vt, half * 16 + 2 * vq + (lane >> 4)), r[0], r[1], r[2], r[3]);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
               dev::mma_f16(o[4 * vq + u], pa0, pa1, pa2, pa3, dev::e4m3x2_to_f16x2(static_cast<uint16_t>(r[u] & 0xFFFFu)),
@@ -683,9 +739,13 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       }
       }
       if constexpr (RAW) {
-        // this warp is done with the page's buffer
+        // this warp is done with the iteration's buffers
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(a_bar + 8 * (NB + buf));
+        if (lane == 0) {
+#pragma unroll
+          for (int u = 0; u < PPI; ++u)
+            if (j + u < seg.num_pages) tc::mbar_arrive(a_bar + 8 * (NB + buf_u[u]));
+        }
       } else {
         __syncthreads();  // s_kv and the exchange buffers are reused by the next page
       }
