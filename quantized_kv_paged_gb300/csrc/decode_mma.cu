@@ -704,13 +704,16 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
               const int b = m;                       // block 2c + m within the four loaded
               const uint32_t s01 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(sw[0], sw[1], b | ((4 + b) << 4))));
               const uint32_t s23 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(sw[2], sw[3], b | ((4 + b) << 4))));
+              // each token's byte converts to {even dim, odd dim}; byte permutes regroup the halves
+              // into token pairs per dim
               const uint32_t x = r[m];
-              const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
-              const uint32_t e01 = (lo & 0xFu) | ((lo >> 4) & 0xF0u), e23 = ((lo >> 16) & 0xFu) | ((lo >> 20) & 0xF0u);
-              const uint32_t o01 = (hi & 0xFu) | ((hi >> 4) & 0xF0u), o23 = ((hi >> 16) & 0xFu) | ((hi >> 20) & 0xF0u);
+              const uint32_t c0 = dev::e2m1x2_to_f16x2(x & 0xFFu), c1 = dev::e2m1x2_to_f16x2((x >> 8) & 0xFFu);
+              const uint32_t c2 = dev::e2m1x2_to_f16x2((x >> 16) & 0xFFu), c3 = dev::e2m1x2_to_f16x2(x >> 24);
               const int nt = 4 * (2 * vq + (m >> 1)) + 2 * (m & 1);
-              dev::mma_f16(o[nt], pa0, pa1, pa2, pa3, dev::nvfp4x2_to_f16x2(e01, s01), dev::nvfp4x2_to_f16x2(e23, s23));
-              dev::mma_f16(o[nt + 1], pa0, pa1, pa2, pa3, dev::nvfp4x2_to_f16x2(o01, s01), dev::nvfp4x2_to_f16x2(o23, s23));
+              dev::mma_f16(o[nt], pa0, pa1, pa2, pa3, dev::hmul2_f16(__byte_perm(c0, c1, 0x5410), s01),
+                           dev::hmul2_f16(__byte_perm(c2, c3, 0x5410), s23));
+              dev::mma_f16(o[nt + 1], pa0, pa1, pa2, pa3, dev::hmul2_f16(__byte_perm(c0, c1, 0x7632), s01),
+                           dev::hmul2_f16(__byte_perm(c2, c3, 0x7632), s23));
             }
           }
         } else if constexpr (RAW) {
