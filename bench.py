@@ -226,8 +226,7 @@ def heads_sweep(q, pk, w, kv, args, steps, g=1.0, min_splits=0, heads=(16, 32, 6
     out = {}
     for h in heads:
         pb = Problem(q, with_heads(w, h), kv, g=g, min_splits=min_splits, algo=args.algo)
-        ms, att = time_problem(pb, steps, args.warmup)
-        r = summarize(pb, ms, att, pk)
+        r = measure(pb, steps, args.warmup, pk)
         t_hbm = pb.kv_bytes / (pk["hbm_gbs"] * 1e9) * 1e6
         t_tc = pb.flops / (pk["bf16_tflops"] * 1e12) * 1e6
         r["binding"] = "hbm" if t_hbm >= t_tc else "tensor"
@@ -284,6 +283,17 @@ def time_problem(pb: Problem, steps: int, warmup: int, world: int = 1):
     ms = t0.elapsed_time(t1) / steps
     attend_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     return ms, attend_ms
+
+
+def measure(pb: Problem, steps: int, warmup: int, pk: dict):
+    """time_problem + summarize for one extra workload line, with the SM clock and any throttle
+    reason sampled over its own timed region."""
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms, att = time_problem(pb, steps, warmup)
+    r = summarize(pb, ms, att, pk)
+    c = clk.summary()
+    r["clocks"] = {"sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons", [])}
+    return r
 
 
 def summarize(pb: Problem, ms: float, attend_ms: float, pk: dict):
@@ -491,8 +501,7 @@ def extra_workloads(q, pk, dev, args, main_w=None):
         res["heads_sweep_mla_fp8_b44_l32k"] = heads_sweep(q, pk, main_w, q.KV_FP8_E4M3, args, steps)
         # the same tokens in the per-token-scaled FP8 layout (580 bytes per token)
         pt = Problem(q, main_w, q.KV_FP8_PER_TOKEN, algo=args.algo)
-        ms, att = time_problem(pt, steps, args.warmup)
-        res["mla_fp8_per_token_b44_h128_l32k"] = summarize(pt, ms, att, pk)
+        res["mla_fp8_per_token_b44_h128_l32k"] = measure(pt, steps, args.warmup, pk)
         del pt
         res["heads_sweep_mla_fp8_per_token_b44_l32k"] = heads_sweep(q, pk, main_w, q.KV_FP8_PER_TOKEN, args, steps,
                                                                    heads=(16,))
@@ -500,8 +509,7 @@ def extra_workloads(q, pk, dev, args, main_w=None):
     # NVFP4, 10 x 163,840 (+1 appended per step), 128 heads
     w = synth.workload("mla_nvfp4_b10_h128_l160k", device=dev)
     pb = Problem(q, w, q.KV_NVFP4, g=1.0, append=True, algo=args.algo)
-    ms, att = time_problem(pb, steps, args.warmup)
-    res["mla_nvfp4_b10_h128_l160k"] = summarize(pb, ms, att, pk)
+    res["mla_nvfp4_b10_h128_l160k"] = measure(pb, steps, args.warmup, pk)
     del pb
     res["heads_sweep_mla_nvfp4_b10_l160k"] = heads_sweep(q, pk, w, q.KV_NVFP4, args, steps)
     nv = Problem(q, w, q.KV_NVFP4, g=1.0)
@@ -513,8 +521,7 @@ def extra_workloads(q, pk, dev, args, main_w=None):
     w = synth.workload("mla_nvfp4_b1_h128_l1m", device=dev)
     for tag, g in (("g1", 1.0), ("calibrated", calibrated_scale(w))):
         pb = Problem(q, w, q.KV_NVFP4, g=g, min_splits=148, algo=args.algo)
-        ms, att = time_problem(pb, steps, args.warmup)
-        r = summarize(pb, ms, att, pk)
+        r = measure(pb, steps, args.warmup, pk)
         r["global_scale"] = g
         res[f"mla_nvfp4_b1_h128_l1m_{tag}"] = r
         del pb
@@ -524,8 +531,8 @@ def extra_workloads(q, pk, dev, args, main_w=None):
     # mixed serving batch: fused FP8 decode vs cast-then-attend (pool cast to BF16 + BF16 decode)
     w = synth.workload("mla_fp8_mixed_b64_h128_pool495552", device=dev)
     fused = Problem(q, w, q.KV_FP8_E4M3, algo=args.algo)
-    ms, att = time_problem(fused, steps, args.warmup)
-    r = summarize(fused, ms, att, pk)
+    r = measure(fused, steps, args.warmup, pk)
+    ms = r["us_per_step"] * 1e-3
     # the baseline's BF16 decode runs with whichever kernel family is faster on it
     best = None
     for algo in (q.ALGO_MMA_SYNC, q.ALGO_TCGEN05):

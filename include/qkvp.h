@@ -104,6 +104,9 @@ typedef struct {
   int32_t max_worker_pages;  /* most pages given to one worker (load balance) */
   int32_t min_worker_pages;  /* fewest pages given to one worker */
   int32_t num_partials;      /* FP32 split partials held in the workspace */
+  int32_t max_request_segments; /* most segments one request is cut into */
+  int32_t num_wide_requests; /* requests cut into more than 8 segments: the combine gives each of
+                                them several CTAs per head instead of one thread per 8 output dims */
   int64_t total_pages;       /* sum over requests of ceil(len / 64) */
   int64_t total_tokens;      /* sum of lengths */
   uint64_t workspace_bytes;  /* device workspace the run needs (table + split partials) */

@@ -32,7 +32,8 @@ class qkvp_plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "num_heads", "page_size", "kv_dtype", "algo", "num_workers", "ctas_per_worker",
         "num_segments", "num_split_requests", "num_empty_requests", "max_worker_pages",
-        "min_worker_pages", "num_partials")] + [
+        "min_worker_pages", "num_partials", "max_request_segments",
+        "num_wide_requests")] + [
         ("total_pages", ctypes.c_int64), ("total_tokens", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_uint64), ("table_bytes", ctypes.c_uint64),
         ("partial_o_offset", ctypes.c_uint64), ("partial_lse_offset", ctypes.c_uint64),

@@ -36,8 +36,8 @@ int query_sms() {
 // request order, and the segments of one request are contiguous.
 struct Split {
   std::vector<Segment> segs;
-  std::vector<int32_t> wptr, rptr;
-  int32_t split_reqs = 0, empty_reqs = 0, max_pages = 0, min_pages = 0, partials = 0;
+  std::vector<int32_t> wptr, rptr, wide;
+  int32_t split_reqs = 0, empty_reqs = 0, max_pages = 0, min_pages = 0, partials = 0, max_req_segs = 0;
   int64_t total_pages = 0, total_tokens = 0;
 };
 
@@ -94,6 +94,8 @@ void split_pages(const int32_t* indptr, const int32_t* len, int batch, int worke
     const size_t n = k - k0;
     if (n == 0) ++s.empty_reqs;
     if (n >= 2) ++s.split_reqs;
+    s.max_req_segs = std::max<int32_t>(s.max_req_segs, static_cast<int32_t>(n));
+    if (n > static_cast<size_t>(kCombineWideSegs)) s.wide.push_back(q);
     for (size_t i = k0; i < k; ++i) s.segs[i].partial = n == 1 ? -1 : part++;
   }
   s.rptr[batch] = static_cast<int32_t>(k);
@@ -204,6 +206,8 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   plan->max_worker_pages = s.max_pages;
   plan->min_worker_pages = s.min_pages;
   plan->num_partials = s.partials;
+  plan->max_request_segments = s.max_req_segs;
+  plan->num_wide_requests = static_cast<int32_t>(s.wide.size());
   plan->total_pages = s.total_pages;
   plan->total_tokens = s.total_tokens;
   plan->table_bytes = t.bytes;
@@ -222,6 +226,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   if (!s.segs.empty()) std::memcpy(blob.data() + t.segs, s.segs.data(), s.segs.size() * sizeof(Segment));
   std::memcpy(blob.data() + t.wptr, s.wptr.data(), s.wptr.size() * 4);
   std::memcpy(blob.data() + t.rptr, s.rptr.data(), s.rptr.size() * 4);
+  if (!s.wide.empty()) std::memcpy(blob.data() + t.wide, s.wide.data(), s.wide.size() * 4);
   cudaError_t e = cudaMemcpyAsync(workspace, blob.data(), blob.size(), cudaMemcpyHostToDevice,
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QKVP_E_CUDA;
@@ -258,6 +263,7 @@ DecodeArgs make_args(const qkvp_plan* plan, const void* q, const void* kv_data, 
   a.segs = reinterpret_cast<const Segment*>(ws + t.segs);
   a.worker_ptr = reinterpret_cast<const int32_t*>(ws + t.wptr);
   a.req_seg_ptr = reinterpret_cast<const int32_t*>(ws + t.rptr);
+  a.wide_req = reinterpret_cast<const int32_t*>(ws + t.wide);
   a.part_o = reinterpret_cast<float*>(ws + plan->partial_o_offset);
   a.part_lse = reinterpret_cast<float*>(ws + plan->partial_lse_offset);
   a.status = reinterpret_cast<int*>(ws + t.status);
@@ -298,10 +304,11 @@ int mla_decode_combine(const qkvp_plan* plan, float global_scale, void* out, flo
   int st = check_run_args(plan, 0, 0.0f, global_scale, workspace, workspace_bytes);
   if (st != QKVP_OK) return st;
   if (plan->batch == 0 || (plan->num_split_requests == 0 && plan->num_empty_requests == 0)) return QKVP_OK;
-  if (!out || !aligned(out, 4) || (lse && !aligned(lse, 4))) return QKVP_E_INVALID;
+  if (!out || !aligned(out, 16) || (lse && !aligned(lse, 4))) return QKVP_E_INVALID;
+  if (plan->num_wide_requests < 0 || plan->num_wide_requests > plan->batch) return QKVP_E_INVALID;
   const DecodeArgs a = make_args(plan, nullptr, nullptr, nullptr, 0, nullptr, 0.0f, global_scale,
                                  out, lse, workspace);
-  cudaError_t e = launch_combine(a, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_combine(a, plan->num_wide_requests, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
 }
 

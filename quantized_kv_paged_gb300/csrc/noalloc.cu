@@ -35,13 +35,14 @@ static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
 std::mutex g_mutex;                     // guards the static host staging and the address cache
 void* g_scratch_addr[kMaxDevices] = {};  // device address of g_scratch, per device
-uint8_t g_table[kMaxSegments * sizeof(Segment) + (kMaxWorkers + 1) * 4 + (kMaxBatch + 1) * 4 + 3 * 256];
+uint8_t g_table[kMaxSegments * sizeof(Segment) + (kMaxWorkers + 1) * 4 + (kMaxBatch + 1) * 4 + kMaxBatch * 4 +
+                4 * 256];
 
 // The same split as mla_decode_plan (requests end to end in page units, worker w takes pages
 // [w * quota, (w + 1) * quota), pieces cut at request boundaries and at `cap` pages), written
 // straight into static arrays. Returns the segment count, or -1 if it exceeds kMaxSegments.
 int64_t split_static(const int32_t* indptr, const int32_t* len, int batch, int workers, int min_splits,
-                     Segment* segs, int32_t* wptr, int32_t* rptr, qkvp_plan* plan) {
+                     Segment* segs, int32_t* wptr, int32_t* rptr, int32_t* wide, qkvp_plan* plan) {
   int64_t total = 0, tokens = 0;
   for (int r = 0; r < batch; ++r) {
     total += (static_cast<int64_t>(len[r]) + kPage - 1) / kPage;
@@ -81,13 +82,15 @@ int64_t split_static(const int32_t* indptr, const int32_t* len, int batch, int w
   }
   wptr[workers] = static_cast<int32_t>(n);
   int64_t k = 0;
-  int32_t part = 0, split = 0, empty = 0;
+  int32_t part = 0, split = 0, empty = 0, most = 0, nwide = 0;
   for (int q = 0; q < batch; ++q) {
     rptr[q] = static_cast<int32_t>(k);
     const int64_t k0 = k;
     while (k < n && segs[k].req == q) ++k;
     if (k == k0) ++empty;
     if (k - k0 >= 2) ++split;
+    most = std::max<int32_t>(most, static_cast<int32_t>(k - k0));
+    if (k - k0 > kCombineWideSegs) wide[nwide++] = q;
     for (int64_t i = k0; i < k; ++i) segs[i].partial = (k - k0 == 1) ? -1 : part++;
   }
   rptr[batch] = static_cast<int32_t>(k);
@@ -95,6 +98,8 @@ int64_t split_static(const int32_t* indptr, const int32_t* len, int batch, int w
   plan->num_split_requests = split;
   plan->num_empty_requests = empty;
   plan->num_partials = part;
+  plan->max_request_segments = most;
+  plan->num_wide_requests = nwide;
   plan->max_worker_pages = max_pages;
   plan->min_worker_pages = min_pages;
   plan->total_pages = total;
@@ -140,9 +145,11 @@ extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* 
   static Segment segs[kMaxSegments];
   static int32_t wptr[kMaxWorkers + 1];
   static int32_t rptr[kMaxBatch + 1];
+  static int32_t wide[kMaxBatch];
   qkvp_plan plan;
   std::memset(&plan, 0, sizeof(plan));
-  const int64_t nseg = split_static(kv_indptr_host, kv_len_host, batch, workers, min_splits, segs, wptr, rptr, &plan);
+  const int64_t nseg = split_static(kv_indptr_host, kv_len_host, batch, workers, min_splits, segs, wptr, rptr, wide,
+                                    &plan);
   if (nseg < 0) return QKVP_E_WORKSPACE;
   const TableLayout t = table_layout(nseg, workers, batch);
   plan.batch = batch;
@@ -163,6 +170,7 @@ extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* 
   if (nseg > 0) std::memcpy(g_table + t.segs, segs, nseg * sizeof(Segment));
   std::memcpy(g_table + t.wptr, wptr, (workers + 1) * 4);
   std::memcpy(g_table + t.rptr, rptr, (batch + 1) * 4);
+  if (plan.num_wide_requests > 0) std::memcpy(g_table + t.wide, wide, plan.num_wide_requests * 4);
 
   // Set-up, once per device, with that device current: the device address of the scratch.
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QKVP_E_CUDA;

@@ -45,6 +45,7 @@ struct DecodeArgs {
   const Segment* segs;
   const int32_t* worker_ptr;  // [num_workers + 1]
   const int32_t* req_seg_ptr; // [batch + 1]
+  const int32_t* wide_req;    // [num_wide] requests with more than kCombineWideSegs segments
   float* part_o;              // [num_segments][H][512]
   float* part_lse;            // [num_segments][H], log2 domain
   uint16_t* out;              // bf16 [B][H][512]
@@ -55,22 +56,28 @@ struct DecodeArgs {
   float out_scale;            // g
 };
 
-// Workspace layout of a plan: the segment table, the per-worker segment ranges and the
-// per-request segment ranges, each 256-byte aligned, followed by the FP32 partials.
+// Workspace layout of a plan: the segment table, the per-worker segment ranges, the per-request
+// segment ranges and the list of wide requests, each 256-byte aligned, followed by the FP32 partials.
 constexpr uint64_t kTableAlign = 256;
 inline uint64_t align_up(uint64_t x) { return (x + kTableAlign - 1) / kTableAlign * kTableAlign; }
 
 // The status word is zero after planning; a kernel that gives up waiting sets bits in it.
 struct TableLayout {
-  uint64_t segs, wptr, rptr, status, bytes;
+  uint64_t segs, wptr, rptr, wide, status, bytes;
 };
+
+// A request cut into more segments than this is merged by the combine's wide CTAs (eight segment
+// groups per quarter head) instead of one thread per 8 output dims walking every segment; the
+// planner lists such requests in the table.
+constexpr int kCombineWideSegs = 8;
 
 inline TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch) {
   TableLayout t;
   t.segs = 0;
   t.wptr = align_up(static_cast<uint64_t>(segments) * sizeof(Segment));
   t.rptr = t.wptr + align_up(static_cast<uint64_t>(workers + 1) * 4);
-  t.status = t.rptr + align_up(static_cast<uint64_t>(batch + 1) * 4);
+  t.wide = t.rptr + align_up(static_cast<uint64_t>(batch + 1) * 4);
+  t.status = t.wide + align_up(static_cast<uint64_t>(batch) * 4);
   t.bytes = t.status + kTableAlign;
   return t;
 }
@@ -100,7 +107,7 @@ cudaError_t launch_encode(const float* x, int64_t n, int fmt, uint8_t* codes, cu
 cudaError_t launch_cast(const uint8_t* in, int64_t n, uint16_t* out, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
-cudaError_t launch_combine(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const DecodeArgs& a, int num_wide, cudaStream_t s);
 
 // Heads per CTA of the mma.sync kernel for a head count (0 if unsupported).
 int mma_heads_per_cta(int heads);

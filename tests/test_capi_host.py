@@ -82,6 +82,9 @@ def test_split_is_balanced_and_covers_every_page(lib):
     assert p.max_worker_pages == -(-p.total_pages // p.num_workers)
     assert p.min_worker_pages >= p.total_pages - (p.num_workers - 1) * p.max_worker_pages
     assert p.num_segments >= 44 and p.workspace_bytes >= p.num_partials * 128 * 512 * 4
+    # a request's 512 contiguous pages meet at most ceil(512 / quota) + 1 worker ranges
+    assert 2 <= p.max_request_segments <= -(-512 // p.max_worker_pages) + 1
+    assert p.num_wide_requests == 0   # every request merges in the narrow combine CTAs
 
 
 def test_min_splits_spreads_one_long_request(lib):
@@ -89,8 +92,9 @@ def test_min_splits_spreads_one_long_request(lib):
     ptr = np.array([0, 16384], np.int32)
     p = plan(ptr, lens, min_splits=148)
     assert p.num_segments >= 148 and p.num_split_requests == 1 and p.num_partials == p.num_segments
+    assert p.max_request_segments == p.num_segments and p.num_wide_requests == 1
     p0 = plan(ptr, lens, min_splits=0)
-    assert p0.num_segments == p0.num_workers
+    assert p0.num_segments == p0.num_workers == p0.max_request_segments
 
 
 def test_ragged_and_empty_requests(lib):
@@ -100,6 +104,13 @@ def test_ragged_and_empty_requests(lib):
     assert p.num_empty_requests == 2
     assert p.total_pages == sum((int(l) + 63) // 64 for l in lens)
     assert p.num_workers == 4 and p.ctas_per_worker == 1
+    assert (p.max_request_segments >= 2) == (p.num_split_requests > 0)
+    assert p.max_request_segments <= p.num_segments
+    assert (p.num_wide_requests > 0) == (p.max_request_segments > 8)
+    # one worker per 16-head CTA group at 16 heads: with 4 workers no request meets more than 4
+    assert p.num_wide_requests == 0
+    pw = plan(ptr, lens, heads=16, sms=152)
+    assert pw.max_request_segments > 8 and 1 <= pw.num_wide_requests <= 2
 
 
 def test_run_and_append_reject_before_launch(lib):
