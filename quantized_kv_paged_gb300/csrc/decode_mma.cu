@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         for (int u = 0; u < PPI; ++u) {
           const int pp = j - PPI + u;
           if (pp + NB < seg.num_pages) {
-            const int pb = pp % NB;
+            const int pb = pp % NBx;
             if (!tc::mbar_wait(a_bar + 8 * (NB + pb), (fills[pb] - 1) & 1)) atomicOr(a.status, 16);
             tc::fence_proxy_async_smem();
             fetch_raw_page<KV>(a, &kv_map, a.kv_indices[seg.page_begin + pp + NB], a_raw + pb * raw_bytes<KV>(),

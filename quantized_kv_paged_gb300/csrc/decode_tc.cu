@@ -129,6 +129,12 @@ __device__ __forceinline__ void ldg_nc32(const void* p, uint32_t (&v)[8]) {
                : "l"(p));
 }
 
+// The same store without a compiler memory barrier: later global loads may be issued before it. Only
+// for shared memory that no ordinary load reads (operands the tensor cores read after a proxy fence).
+__device__ __forceinline__ void sts128_relaxed(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
@@ -527,48 +533,63 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
   for (int g = 0; !cur.done(); ++g) {
     const Segment seg = cur.seg;
     if (cur.j == 0 && seg.req != cur_req) {
-      // ---- Q row of head h (QK of the previous page has completed: its logits were read). A
-      // power of two 2^-sh from the row's largest |q| (the same in both CTAs) keeps every value
-      // inside FP16; 2^sh joins this row's logit scale ----
+      // ---- Q row of head h (QK of the previous page has completed: its logits were read) ----
       // With fewer than 128 query heads the rows h >= heads hold zeros: their logits are 0, their
       // softmax runs on them harmlessly and nothing of theirs is written.
+      // BF16 -> FP16 is exact for magnitudes in [2^-14, 2^15): the row is converted unscaled. A warp
+      // holding a row with a value of 2^15 or more (or inf / NaN) converts again, with each such row
+      // scaled by 2^-sh from its largest |q| (which then lies in [2^14, 2^15)); 2^sh joins the row's
+      // logit scale. Both CTAs of the pair take the same decisions. Elements below 2^-14 become FP16
+      // subnormals (flushed to zero below 2^-25); an unscaled row loses nothing else.
       const bool live = h < a.heads;
       const uint8_t* qrow = reinterpret_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(seg.req) * a.heads + (live ? h : 0)) * (kLatent * 2);
-      uint32_t mx = 0;
-      for (int i = 0; live && i < kLatent * 2 / 16; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + 16 * i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
-      }
-      int sh = 0;
-      if (mx != 0u && mx < 0x7F80u) sh = max(-100, min(113, static_cast<int>(mx >> 7) - 127 - 14));
-      const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-      q_scale = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
       // latent dim of position d in this CTA's contraction order (own nope dims, other nope dims, rope)
       auto perm = [c](int d) { return d < 256 ? 256 * c + d : (d < 512 ? 256 * (1 - c) + d - 256 : d); };
+      auto big = [](uint32_t w) { return (w & 0x7FFFu) >= 0x4700u || ((w >> 16) & 0x7FFFu) >= 0x4700u; };
+      float down = 1.0f;
+      q_scale = a.scale_log2;
 #pragma unroll 1
-      for (int part = 0; part < kQTmemDims / 64; ++part) {   // 64 dims -> 32 TMEM columns
-        uint32_t r[32];
-        const uint8_t* src = qrow + perm(64 * part) * 2;
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        bool hot = false;
+#pragma unroll 1
+        for (int part = 0; part < kQTmemDims / 64; ++part) {   // 64 dims -> 32 TMEM columns
+          uint32_t r[32];
+          const uint8_t* src = qrow + perm(64 * part) * 2;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = live ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
-          r[4 * i] = dev::bf16x2_to_f16x2(v.x, down);
-          r[4 * i + 1] = dev::bf16x2_to_f16x2(v.y, down);
-          r[4 * i + 2] = dev::bf16x2_to_f16x2(v.z, down);
-          r[4 * i + 3] = dev::bf16x2_to_f16x2(v.w, down);
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = live ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
+            hot |= big(v.x) || big(v.y) || big(v.z) || big(v.w);
+            r[4 * i] = dev::bf16x2_to_f16x2(v.x, down);
+            r[4 * i + 1] = dev::bf16x2_to_f16x2(v.y, down);
+            r[4 * i + 2] = dev::bf16x2_to_f16x2(v.z, down);
+            r[4 * i + 3] = dev::bf16x2_to_f16x2(v.w, down);
+          }
+          __syncwarp();
+          tc::tmem_st32<false>(tl + TM_Q + 32 * part, r);   // the next part's loads may go first
         }
-        __syncwarp();
-        tc::tmem_st32(tl + TM_Q + 32 * part, r);
-      }
 #pragma unroll
-      for (int i = 0; i < 8 * kQSmemAtoms; ++i) {     // positions 384..575 -> 64-dim atoms, row h
-        const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + (perm(kQTmemDims + 64 * (i >> 3)) + 8 * (i & 7)) * 2)
-                             : make_uint4(0, 0, 0, 0);
-        sts128(qs + (i >> 3) * kQAtom + tc::sw128_offset(h, i & 7),
-               make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
-                          dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
+        for (int i = 0; i < 8 * kQSmemAtoms; ++i) {     // positions 384..575 -> 64-dim atoms, row h
+          const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + (perm(kQTmemDims + 64 * (i >> 3)) + 8 * (i & 7)) * 2)
+                               : make_uint4(0, 0, 0, 0);
+          hot |= big(v.x) || big(v.y) || big(v.z) || big(v.w);
+          sts128_relaxed(qs + (i >> 3) * kQAtom + tc::sw128_offset(h, i & 7),
+                         make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
+                                    dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
+        }
+        if (attempt == 1 || !__any_sync(0xffffffffu, hot)) break;
+        if (hot) {                                      // this row: its largest |q|
+          uint32_t mx = 0;
+          for (int i = 0; i < kLatent * 2 / 16; ++i) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + 16 * i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+          }
+          int sh = 0;
+          if (mx < 0x7F80u) sh = max(-100, min(113, static_cast<int>(mx >> 7) - 127 - 14));
+          down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+          q_scale = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+        }
       }
       tc::tmem_wait_st();
       tc::fence_proxy_async_smem();

@@ -1,6 +1,8 @@
 """The tcgen05 (TMEM, CTA-pair) decode kernel against the FP64 oracle: ragged batches split over
 different SM counts, every pool dtype, forced rescales of the running maximum, and the full-size
 workloads on sampled (request, head) pairs in the launch configuration the benchmark times."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -42,6 +44,29 @@ def test_tc_fewer_heads_ride_as_zero_rows(qkvp, heads):
     for kv in (FP8, NVFP4):
         stats, plan = _run(w, kv, g=1.0 if kv != NVFP4 else 0.37, num_sms=37)
         assert plan.algo == TC
+
+
+@pytest.mark.parametrize("algo", [TC, q.ALGO_MMA_SYNC])
+def test_q_rows_outside_the_unscaled_fp16_range(qkvp, algo):
+    """Rows holding a value of 2^15 or more (the whole row, or one element) are rescaled before the
+    FP16 conversion; rows whose values sit below 1 or at 2^-40, and a row just under 2^15, are not.
+    Both kernels, against the FP64 oracle."""
+    lens = [300, 64, 1000]
+    w = synth.build_workload("qrange", lens, heads=128, pool_pages=40, seed=11, outliers=4, device="cuda",
+                             extra_pages=[1] * len(lens))
+    x = w.q.float()
+    x[0, 3] *= 2.0 ** 14            # largest |q| around 2^15.6
+    x[0, 9, 17] = 40000.0           # one element above 2^15
+    x[1, 77] *= 2.0 ** -12          # largest |q| below 1
+    x[2, 100] *= 2.0 ** -40         # tiny row
+    x[2, 5] *= 2.0 ** 13            # largest |q| just under 2^15: unscaled
+    w = dataclasses.replace(w, q=x.to(torch.bfloat16))
+    for kv in (FP8, NVFP4):
+        g = 1.0 if kv != NVFP4 else 0.37
+        out, lse, plan = gpu_decode(w, kv, gpu_pools(w, kv, g), g, algo=algo, num_sms=37)
+        o_ref, lse_ref = oracle_decode(w, kv, oracle_pools(w, kv, g), g)
+        compare(out.float().cpu().numpy().reshape(-1, 512), lse.cpu().numpy().reshape(-1), o_ref, lse_ref)
+        assert plan.algo == algo
 
 
 def test_tc_tiny_single_page(qkvp):
