@@ -17,8 +17,9 @@
  *  - Decode reads the quantized pages directly and dequantizes inside the kernel; nothing casts the
  *    pool to BF16 first (same page, section "SGLang implementation", item 3).
  *
- * Memory layout (all device buffers are caller-owned; the library allocates no device memory and
- * keeps no global mutable state):
+ * Memory layout (all device buffers are caller-owned; the library allocates no device memory. Its
+ * only global state is host-side: per device, four pinned staging buffers and events for the work
+ * table upload of mla_decode_plan, and the fixed scratch of mla_decode_noalloc):
  *  - slot s = page * page_size + offset; page_size must be 64.
  *  - FP8 pool  : kv_data uint8 [num_pages][64][576], one E4M3 byte per latent element. The decode
  *                entry points read kv_data (any pool type) with 32-byte loads: it must be 32-byte aligned.
@@ -171,8 +172,11 @@ int kv_append_quant(const void* src, int32_t src_dtype, int64_t n_tokens,
  *  algo           a qkvp_algo; QKVP_ALGO_AUTO picks the fastest supported family.
  *  workspace      device buffer that receives the work table; NULL makes this a pure host query
  *                 that only fills *plan (including plan->workspace_bytes) and touches no device.
- *  stream         stream of the table upload (an asynchronous copy from library-owned staging, so
- *                 the host arrays may be reused as soon as this returns).
+ *  stream         stream of the table upload: an asynchronous copy from one of four library-owned
+ *                 pinned buffers (per device, reused once its previous copy has completed), so the
+ *                 call does not wait for earlier work on the stream and the host arrays may be
+ *                 reused as soon as it returns. During stream capture, or if pinned memory is
+ *                 refused, it copies from pageable memory instead.
  *
  * Returns QKVP_E_WORKSPACE (with plan->workspace_bytes filled) when workspace is non-NULL but
  * smaller than needed.

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "../../include/qkvp.h"
@@ -18,6 +19,57 @@ namespace {
 constexpr uint64_t kAlign = kTableAlign;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Pinned host staging for work-table uploads, per device: a small ring of buffers, each with an
+// event recorded after its copy. A copy from pageable memory can hold the calling thread until the
+// stream's earlier work has drained, which serialises a host loop of plan + decode with the GPU;
+// from pinned memory the copy is queued and the call returns. A slot is reused only after its
+// previous copy has completed (its event). The buffers live until the process exits.
+constexpr int kStageDevices = 64, kStageSlots = 4;
+constexpr size_t kStageMinBytes = 64 << 10;
+struct StageSlot {
+  void* host = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;
+};
+std::mutex g_stage_mutex;
+StageSlot g_stage[kStageDevices][kStageSlots];
+int g_stage_next[kStageDevices] = {};
+
+// Copies n bytes to the device buffer dst in stream order. Pinned staging where it can; a pageable
+// copy during stream capture (an event cannot be waited on there) or if pinned memory is refused.
+cudaError_t upload_table(void* dst, const void* src, size_t n, cudaStream_t st) {
+  int dev = -1;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kStageDevices &&
+      cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
+    std::lock_guard<std::mutex> lock(g_stage_mutex);
+    StageSlot& slot = g_stage[dev][g_stage_next[dev]];
+    bool ok = true;
+    if (slot.done && cudaEventSynchronize(slot.done) != cudaSuccess) ok = false;
+    if (ok && slot.cap < n) {
+      if (slot.host) cudaFreeHost(slot.host);
+      slot.host = nullptr;
+      slot.cap = 0;
+      const size_t want = n > kStageMinBytes ? n : kStageMinBytes;
+      if (cudaHostAlloc(&slot.host, want, cudaHostAllocPortable) == cudaSuccess) slot.cap = want;
+      else { slot.host = nullptr; ok = false; }
+    }
+    if (ok && !slot.done && cudaEventCreateWithFlags(&slot.done, cudaEventDisableTiming) != cudaSuccess) {
+      slot.done = nullptr;
+      ok = false;
+    }
+    if (ok) {
+      std::memcpy(slot.host, src, n);
+      cudaError_t e = cudaMemcpyAsync(dst, slot.host, n, cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess) e = cudaEventRecord(slot.done, st);
+      g_stage_next[dev] = (g_stage_next[dev] + 1) % kStageSlots;
+      return e;
+    }
+    cudaGetLastError();   // a refused pinned allocation is not an error of this call
+  }
+  return cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st);
+}
 
 int query_sms() {
   int dev = 0, sms = 0;
@@ -227,8 +279,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   std::memcpy(blob.data() + t.wptr, s.wptr.data(), s.wptr.size() * 4);
   std::memcpy(blob.data() + t.rptr, s.rptr.data(), s.rptr.size() * 4);
   if (!s.wide.empty()) std::memcpy(blob.data() + t.wide, s.wide.data(), s.wide.size() * 4);
-  cudaError_t e = cudaMemcpyAsync(workspace, blob.data(), blob.size(), cudaMemcpyHostToDevice,
-                                  reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = upload_table(workspace, blob.data(), blob.size(), reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QKVP_E_CUDA;
   plan->magic = kPlanMagic;
   return QKVP_OK;
