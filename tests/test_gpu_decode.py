@@ -89,6 +89,43 @@ def test_nvfp4_scale_folding(qkvp):
         _run(w, NVFP4, g=g, num_sms=8)
 
 
+@pytest.mark.parametrize("algo", [q.ALGO_MMA_SYNC, q.ALGO_TCGEN05])
+def test_plan_uploads_in_flight(qkvp, algo):
+    """Six plans of different lengths are uploaded into six workspaces and decoded with no host
+    synchronisation in between, queued behind a few milliseconds of other GPU work, so more table
+    uploads are in flight than the library has pinned staging buffers (four). Each result equals the
+    same plan decoded with a synchronisation after every call, bit for bit."""
+    w = synth.build_workload("flight", [700, 64, 1300, 5, 300], heads=32, pool_pages=60, seed=21, outliers=2,
+                             device="cuda", extra_pages=[1] * 5)
+    pools = gpu_pools(w, FP8)
+    idx = torch.from_numpy(w.kv_indices).to("cuda")
+    cases = [np.maximum(w.kv_len - 3 * k, 0).astype(np.int32) for k in range(6)]
+
+    def workspace(lens):
+        p = q.mla_decode_plan(w.kv_indptr, lens, w.heads, FP8, num_sms=37, algo=algo)
+        return torch.empty(max(p.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+
+    def decode(lens, ws):
+        out = torch.empty((w.batch, w.heads, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.batch, w.heads), dtype=torch.float32, device="cuda")
+        p = q.mla_decode_plan(w.kv_indptr, lens, w.heads, FP8, num_sms=37, algo=algo, workspace=ws)
+        q.mla_decode_run(p, w.q, pools[0], pools[1], w.num_pages, idx, w.sm_scale, 1.0, out, lse, ws)
+        return out, lse
+
+    wss = [workspace(lens) for lens in cases]
+    ref = []
+    for lens, ws in zip(cases, wss):
+        ref.append(decode(lens, ws))
+        torch.cuda.synchronize()
+    a = torch.randn(4096, 4096, device="cuda")
+    for _ in range(20):
+        a = a @ a / 64.0                       # keeps the stream busy while the uploads queue
+    got = [decode(lens, ws) for lens, ws in zip(cases, wss)]
+    torch.cuda.synchronize()
+    for (o, l), (ro, rl) in zip(got, ref):
+        assert torch.equal(o, ro) and torch.equal(l, rl)
+
+
 # ---- full sizes, bench launch configuration, sampled outputs --------------------------------------
 
 def _sample_pairs(w, n, seed):
