@@ -250,13 +250,17 @@ template <> struct Dequant<KV_FP8PT> {
 };
 
 template <> struct Dequant<KV_NVFP4> {
-  // 32 dims (16 packed bytes, two scale blocks) per item, 2 items per atom row
-  static constexpr int kOwn = 32 * 18, kItems = kOwn + 32 * 8;
+  // 64 dims per item: 32 packed bytes in one 32-byte load and the four block scales in one 4-byte
+  // load; one item fills one atom row (own 32 rows x 9 atoms, other 32 rows x 4). Items of 32 dims
+  // took one 16-byte and one 2-byte load each, twice the load instructions for the same bytes.
+  // A warp's 32 items are the 32 rows of one atom, so each of the 8 row stores hits eight distinct
+  // bank groups per eight lanes.
+  static constexpr int kOwn = 32 * 9, kItems = kOwn + 32 * 4;
   static constexpr int kIters = (kItems + kDQ - 1) / kDQ;
-  struct Raw { uint4 v[kIters]; uint32_t s[kIters]; };
+  struct Raw { uint32_t v[kIters][8]; uint32_t s[kIters]; };
   __device__ static Item at(int q, int c) {
     const int qq = q < kOwn ? q : q - kOwn;
-    return item_at(kOwn, q, c, 64, 32 * (qq & 1), ((qq >> 3) & 7) * 4 + ((qq >> 1) & 3));
+    return item_at(kOwn, q, c, 32, 0, qq & 31);
   }
   __device__ static void load(Raw& r, const DecodeArgs& a, int64_t page, int valid, int c, int t) {
     const uint8_t* base = a.kv + page * (kPage * kPacked);
@@ -266,8 +270,8 @@ template <> struct Dequant<KV_NVFP4> {
       const int q = t + kDQ * i;
       const Item it = at(q, c);
       if (q < kItems && it.tok < valid) {
-        r.v[i] = ldg_nc(base + it.tok * kPacked + it.dim / 2);
-        r.s[i] = *reinterpret_cast<const uint16_t*>(sbase + it.tok * kScales + it.dim / 16);
+        ldg_nc32(base + it.tok * kPacked + it.dim / 2, r.v[i]);
+        r.s[i] = *reinterpret_cast<const uint32_t*>(sbase + it.tok * kScales + it.dim / 16);
       }
     }
   }
@@ -278,22 +282,24 @@ template <> struct Dequant<KV_NVFP4> {
       const int q = t + kDQ * i;
       if (q >= kItems) continue;
       const Item it = at(q, c);
-      uint32_t o[16];
+      uint32_t o[32];
       if (it.tok < valid) {
-        const uint32_t sa = r.s[i] & 0xFFu, sb = (r.s[i] >> 8) & 0xFFu;
-        const uint32_t ha = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sa | (sa << 8)));
-        const uint32_t hb = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
-        const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
+        uint32_t h[4];
 #pragma unroll
-        for (int b = 0; b < 16; ++b) o[b] = dev::nvfp4x2_to_f16x2((w[b >> 2] >> (8 * (b & 3))) & 0xFFu, b < 8 ? ha : hb);
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t sk = (r.s[i] >> (8 * k)) & 0xFFu;
+          h[k] = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sk | (sk << 8)));
+        }
+#pragma unroll
+        for (int b = 0; b < 32; ++b) o[b] = dev::nvfp4x2_to_f16x2((r.v[i][b >> 2] >> (8 * (b & 3))) & 0xFFu, h[b >> 3]);
       } else {
 #pragma unroll
-        for (int b = 0; b < 16; ++b) o[b] = 0;
+        for (int b = 0; b < 32; ++b) o[b] = 0;
       }
-      const uint32_t ch = ((it.dim & 63) >> 3), at = (it.in_v ? vs : ks) + it.off;
+      const uint32_t at = (it.in_v ? vs : ks) + it.off;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        sts128(at + tc::sw128_offset(it.row, ch + u), make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
+      for (int u = 0; u < 8; ++u)
+        sts128(at + tc::sw128_offset(it.row, u), make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
     }
   }
 };
