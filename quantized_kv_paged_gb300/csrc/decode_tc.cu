@@ -64,7 +64,7 @@ constexpr uint32_t kAtom = 4096;             // 32 token rows x 64 dims FP16, 12
 // and of the other 32 tokens (P.V only): 8 atoms, freed when P.V completes.
 constexpr int kKSlots = 2, kVSlots = 3;
 // Pages ahead that the dequant role prefetches into L2. Measured on one GB300: FP8 pools gain (44 x 32K:
-// 547 -> 539 us); pools whose dequant warps do more per byte lose (NVFP4 10 x 160K: 827 -> 870 us,
+// 547 -> 539 us); pools whose dequant warps do more per byte lose (NVFP4 10 x 160K: 724 -> 747 us,
 // per-token-scaled FP8 44 x 32K: 635 -> 679 us), and BF16 pools are unchanged. So FP8 only.
 template <int KV>
 constexpr int prefetch_ahead() { return KV == KV_FP8 ? 4 : 0; }
