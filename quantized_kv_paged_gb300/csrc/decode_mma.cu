@@ -225,8 +225,10 @@ __device__ __forceinline__ void dequant_page(const uint8_t* s_raw, uint8_t* s_kv
       uint32_t o[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
+        uint32_t c4[4];
+        dev::e2m1x8_to_f16x2x4(w[k], c4);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) o[4 * k + b] = dev::nvfp4x2_to_f16x2((w[k] >> (8 * b)) & 0xFFu, k < 2 ? ha : hb);
+        for (int b = 0; b < 4; ++b) o[4 * k + b] = dev::hmul2_f16(c4[b], k < 2 ? ha : hb);
       }
       uint4* dst = reinterpret_cast<uint4*>(s_kv + row * kRowBytes + ch * 64);
       dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -532,12 +534,13 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
                 if (2 * cb + u >= kChunks) continue;
                 const uint32_t sb = sc[mytok * kScales + 2 * (half * 9 + 2 * cb + u) + (t4 >> 1)];
                 const uint32_t sh2 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
-                const uint32_t w = r[u];
+                uint32_t c4[4];
+                dev::e2m1x8_to_f16x2x4(r[u], c4);
                 dev::mma_f16(s[2 * p + jj], aq[2 * u][0], aq[2 * u][1], aq[2 * u][2], aq[2 * u][3],
-                             dev::nvfp4x2_to_f16x2(w & 0xFFu, sh2), dev::nvfp4x2_to_f16x2((w >> 8) & 0xFFu, sh2));
+                             dev::hmul2_f16(c4[0], sh2), dev::hmul2_f16(c4[1], sh2));
                 dev::mma_f16(kSplit ? s2[kSplit ? 2 * p + jj : 0] : s[2 * p + jj],
                              aq[2 * u + 1][0], aq[2 * u + 1][1], aq[2 * u + 1][2], aq[2 * u + 1][3],
-                             dev::nvfp4x2_to_f16x2((w >> 16) & 0xFFu, sh2), dev::nvfp4x2_to_f16x2(w >> 24, sh2));
+                             dev::hmul2_f16(c4[2], sh2), dev::hmul2_f16(c4[3], sh2));
               }
             }
         }
