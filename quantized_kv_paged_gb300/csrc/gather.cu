@@ -42,18 +42,24 @@ __device__ __forceinline__ uint4 nvfp4_block_to_e4m3(uint2 d, uint32_t s8, float
     // s * e has at most 6 significant bits within [2^-10, 2688]: exact in FP16, so one FP16x2
     // multiply and one FP16x2 -> E4M3x2 conversion (RNE, satfinite) per pair
     const uint32_t s2 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(s8 | (s8 << 8)));
+    uint32_t c0[4], c1[4];                    // code pairs from byte registers
+    dev::e2m1x8_to_f16x2x4(w[0], c0);
+    dev::e2m1x8_to_f16x2x4(w[1], c1);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t v2 = dev::hmul2_f16(dev::e2m1x2_to_f16x2((w[k >> 2] >> (8 * (k & 3))) & 0xFFu), s2);
+      const uint32_t v2 = dev::hmul2_f16(k < 4 ? c0[k] : c1[k - 4], s2);
       bytes[k >> 1] |= dev::f16x2_to_e4m3x2(v2) << (16 * (k & 1));
     }
   } else {
     // the exact product in FP16x2, widened to FP32, one FP32 multiply by g per element, one
     // conversion per pair (RNE, satfinite; no NaN can reach it: NaN scales were handled above)
     const uint32_t s2 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(s8 | (s8 << 8)));
+    uint32_t c0[4], c1[4];                    // packed byte k: elements 2k (low nibble), 2k + 1
+    dev::e2m1x8_to_f16x2x4(w[0], c0);
+    dev::e2m1x8_to_f16x2x4(w[1], c1);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {             // packed byte k: elements 2k (low nibble), 2k + 1
-      const uint32_t v2 = dev::hmul2_f16(dev::e2m1x2_to_f16x2((w[k >> 2] >> (8 * (k & 3))) & 0xFFu), s2);
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t v2 = dev::hmul2_f16(k < 4 ? c0[k] : c1[k - 4], s2);
       const float v0 = __fmul_rn(f16_low(v2), g), v1 = __fmul_rn(f16_high(v2), g);
       bytes[k >> 1] |= dev::f32x2_to_e4m3x2(v0, v1) << (16 * (k & 1));
     }
