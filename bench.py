@@ -163,7 +163,7 @@ def calibrated_scale(w):
 class Problem:
     """A workload resident on the GPU with its plan, workspace and outputs."""
 
-    def __init__(self, q, w, kv, g=1.0, min_splits=0, algo=0, append=False, bf16_pool=False):
+    def __init__(self, q, w, kv, g=1.0, min_splits=0, algo=0, append=False):
         self.q, self.w, self.kv, self.g, self.append = q, w, kv, g, append
         dev = w.pool_fp8.device
         self.dev = dev
