@@ -709,9 +709,9 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
               const uint32_t s23 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(__byte_perm(sw[2], sw[3], b | ((4 + b) << 4))));
               // each token's byte converts to {even dim, odd dim}; byte permutes regroup the halves
               // into token pairs per dim
-              const uint32_t x = r[m];
-              const uint32_t c0 = dev::e2m1x2_to_f16x2(x & 0xFFu), c1 = dev::e2m1x2_to_f16x2((x >> 8) & 0xFFu);
-              const uint32_t c2 = dev::e2m1x2_to_f16x2((x >> 16) & 0xFFu), c3 = dev::e2m1x2_to_f16x2(x >> 24);
+              uint32_t cc[4];
+              dev::e2m1x8_to_f16x2x4(r[m], cc);
+              const uint32_t c0 = cc[0], c1 = cc[1], c2 = cc[2], c3 = cc[3];
               const int nt = 4 * (2 * vq + (m >> 1)) + 2 * (m & 1);
               dev::mma_f16(o[nt], pa0, pa1, pa2, pa3, dev::hmul2_f16(__byte_perm(c0, c1, 0x5410), s01),
                            dev::hmul2_f16(__byte_perm(c2, c3, 0x5410), s23));
