@@ -1,0 +1,68 @@
+"""The benchmark's multi-process path on CPU: two ranks over gloo (127.0.0.1). Decode shards by
+request with no exchange step, so the only collectives are the timing barrier and the max over ranks
+of the step time; the reference arm runs on rank 0 alone."""
+import os
+import socket
+import subprocess
+import sys
+
+import torch
+import torch.multiprocessing as mp
+
+from tests.conftest import ROOT
+
+
+def _free_port() -> int:
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank: int, world: int, port: int, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world), RANK=str(rank),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, r, local = bench.dist_setup()
+        assert (w, r, local) == (world, rank, rank)
+        bench.barrier(world)
+        # every rank times its own replica; the job's time is the slowest rank's
+        t = bench.max_over_ranks(1.5 + rank, world, torch.device("cpu"))
+        out[rank] = t
+        bench.barrier(world)
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+def test_two_ranks_agree_on_the_slowest_time():
+    world = 2
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(timeout=120)
+        codes = [p.exitcode for p in procs]
+        assert codes == [0, 0], codes
+        assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.25, 1, torch.device("cpu")) == 3.25
+    bench.barrier(1)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm's other ranks exit 0 at once, printing nothing."""
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
