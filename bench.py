@@ -198,6 +198,20 @@ class Problem:
         self.flops = self.tokens * w.heads * FLOPS_PER_TOKEN_HEAD
         self.needs_combine = self.plan.num_split_requests > 0 or self.plan.num_empty_requests > 0
 
+    def status(self) -> int:
+        """The plan's device status word: non-zero if a decode kernel gave up waiting on its own
+        pipeline during any step since the plan was uploaded (its outputs are then undefined)."""
+        o = int(self.plan.status_offset)
+        return int(self.ws[o:o + 4].view(torch.int32).item())
+
+    def check(self, what: str):
+        """Refuses the measurement if any timed step's decode kernel gave up."""
+        torch.cuda.synchronize()
+        st = self.status()
+        if st != 0:
+            raise RuntimeError(f"{what}: the decode kernel reported status {st:#x} (a pipeline wait expired); "
+                               "the timed steps did not compute the result, so no number is reported")
+
     def launches_per_step(self):
         return (1 if self.append else 0) + 1 + (1 if self.needs_combine else 0)
 
@@ -220,9 +234,9 @@ def with_heads(w, heads: int):
 
 
 def heads_sweep(q, pk, w, kv, args, steps, g=1.0, min_splits=0, heads=(16, 32, 64)):
-    """Decode of one workload shape at fewer query heads. Below 128 heads the mma.sync kernel runs
-    (the tcgen05 kernel needs 128), and the KV bytes stay the same while the flops shrink, so the
-    step moves from the tensor-bound to the HBM-bound side of the roofline."""
+    """Decode of one workload shape at fewer query heads, with the kernel family the planner picks for
+    that head count. The KV bytes stay the same while the flops shrink, so the step moves from the
+    tensor-bound to the HBM-bound side of the roofline."""
     out = {}
     for h in heads:
         pb = Problem(q, with_heads(w, h), kv, g=g, min_splits=min_splits, algo=args.algo)
@@ -290,6 +304,7 @@ def measure(pb: Problem, steps: int, warmup: int, pk: dict):
     reason sampled over its own timed region."""
     with ClockSampler(torch.cuda.current_device()) as clk:
         ms, att = time_problem(pb, steps, warmup)
+    pb.check(f"{pb.w.name} ({pb.w.heads} heads)")
     r = summarize(pb, ms, att, pk)
     c = clk.summary()
     r["clocks"] = {"sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons", [])}
@@ -376,8 +391,17 @@ def e2e_main(q, pb: Problem, steps: int, warmup: int):
         torch.cuda.synchronize()
         return (time.perf_counter() - t) / steps, p
 
+    def check_ws():
+        torch.cuda.synchronize()
+        for b in range(2):
+            st = int(ws[b][pb.plan.status_offset:pb.plan.status_offset + 4].view(torch.int32).item())
+            if st != 0:
+                raise RuntimeError(f"end-to-end leg: the decode kernel reported status {st:#x}")
+
     s_serial, _ = timed(serial)
+    check_ws()
     s, p = timed(overlapped)
+    check_ws()
     # outside the timed region: the last two results that came back match a plain decode, bit for bit
     pb.step()
     torch.cuda.synchronize()
@@ -393,8 +417,17 @@ def e2e_main(q, pb: Problem, steps: int, warmup: int):
                            "us_per_step": round(s_serial * 1e6, 1)}}
 
 
-def oracle_sample(w, host_pool, kv=1, g=1.0, budget_s=15.0, lens=None):
-    """Time the FP64 oracle on whole requests (all heads) of the workload until ~budget_s."""
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 0.5 * 2.0 ** (e - 7)
+
+
+def oracle_sample(w, host_pool, kv=1, g=1.0, budget_s=15.0, lens=None, out=None, lse=None):
+    """Time the FP64 oracle on whole requests (all heads) of the workload until ~budget_s. When the
+    benchmark's own last output (out [B, H, 512], lse [B, H]) is given, the oracle's results for those
+    requests are compared with it under the parity tolerance (max-abs 2e-2 and mean-abs 2e-3 on the
+    excess over half a BF16 ulp of the FP64 value; lse within 2e-3 + 1e-4 relative): a result that
+    fails refuses the benchmark line."""
     import oracle
     qb = w.q.cpu().view(torch.int16).numpy().view(np.uint16)
     lens = w.kv_len if lens is None else lens
@@ -402,19 +435,33 @@ def oracle_sample(w, host_pool, kv=1, g=1.0, budget_s=15.0, lens=None):
     done_pairs, t_total = 0, 0.0
     H = w.heads
     r = 0
+    worst = {"excess_max": 0.0, "excess_mean_max": 0.0, "lse_max": 0.0}
     while t_total < budget_s and r < w.batch:
         pairs = np.array([[r, h] for h in range(H)], np.int32)
         t = time.perf_counter()
-        oracle.mla_decode(qb, host_pool[0], host_pool[1], kv, 64, w.num_pages, w.kv_indptr, w.kv_indices,
-                          lens, w.sm_scale, g, pairs)
+        o_ref, l_ref = oracle.mla_decode(qb, host_pool[0], host_pool[1], kv, 64, w.num_pages, w.kv_indptr,
+                                         w.kv_indices, lens, w.sm_scale, g, pairs)
         t_total += time.perf_counter() - t
+        if out is not None:
+            ex = np.maximum(0.0, np.abs(out[r].astype(np.float64) - o_ref) - half_ulp_bf16(o_ref))
+            dl = np.abs(lse[r].astype(np.float64) - l_ref)
+            worst["excess_max"] = max(worst["excess_max"], float(ex.max()))
+            worst["excess_mean_max"] = max(worst["excess_mean_max"], float(ex.mean()))
+            worst["lse_max"] = max(worst["lse_max"], float(dl.max()))
+            if not (np.isfinite(out[r]).all() and ex.max() <= 2e-2 and ex.mean() <= 2e-3
+                    and np.all(dl <= 2e-3 + 1e-4 * np.abs(l_ref))):
+                raise RuntimeError(f"request {r}: the benchmark's output differs from the FP64 oracle beyond "
+                                   f"the tolerance ({worst})")
         done_pairs += H
         r += 1
     req = done_pairs / H
     bytes_ = sum(int(lens[i]) for i in range(r)) * LATENT
-    return {"value": round(bytes_ / t_total / 1e9, 4), "unit": "GB/s", "cores": n_threads, "kind": "oracle",
-            "sample": f"{int(req)} of {w.batch} requests x {H} heads of {w.name} ({t_total:.1f} s)",
-            "us_per_step_equivalent": round(t_total / req * w.batch * 1e6, 1)}
+    res = {"value": round(bytes_ / t_total / 1e9, 4), "unit": "GB/s", "cores": n_threads, "kind": "oracle",
+           "sample": f"{int(req)} of {w.batch} requests x {H} heads of {w.name} ({t_total:.1f} s)",
+           "us_per_step_equivalent": round(t_total / req * w.batch * 1e6, 1)}
+    if out is not None:
+        res["checked_against_last_timed_step"] = {k: round(v, 6) for k, v in worst.items()}
+    return res
 
 
 def run_reference(args):
@@ -472,8 +519,16 @@ def main():
                     help="query heads of the timed workload (128 is the headline; fewer for profiling the few-heads path)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
+    ap.add_argument("--profile", default=None, metavar="WORKLOAD",
+                    help="profiling run: time only this workload's decode step (with --heads, --kv, --algo) "
+                         "and print a short summary instead of the benchmark line")
+    ap.add_argument("--kv", default="fp8", choices=["fp8", "nvfp4", "fp8_per_token", "bf16"],
+                    help="pool type of the --profile workload")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.profile:
+        profile_main(args)
+        return
 
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -497,6 +552,9 @@ def main():
     torch.cuda.empty_cache()          # drop the generator's temporaries before timing / profiling
     with ClockSampler(local) as clk:
         ms, attend_ms = time_problem(pb, args.steps, args.warmup, world)
+    pb.check("headline")
+    out_last = pb.out.float().cpu().numpy()      # the last timed step's result, for the oracle leg
+    lse_last = pb.lse.cpu().numpy()
     ms_max = max_over_ranks(ms, world, dev)
     value = world * pb.kv_bytes / (ms_max * 1e-3) / 1e9
     main_stats = summarize(pb, ms, attend_ms, pk)
@@ -517,7 +575,7 @@ def main():
         extra = extra_workloads(q, pk, dev, args, main_w=w)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = oracle_sample(w, (w.pool_fp8.cpu().numpy(), None))
+        cpu = oracle_sample(w, (w.pool_fp8.cpu().numpy(), None), out=out_last, lse=lse_last)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "us_per_step": round(ms_max * 1e3, 2),
@@ -540,6 +598,31 @@ def main():
                 f.write(s + "\n")
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def profile_main(args):
+    """One workload's decode step alone (no end-to-end leg, no extra workloads, no oracle): the
+    command that the ncu captures under profiles/ run."""
+    import quantized_kv_paged_gb300 as q
+    q.load()
+    pk = peaks()
+    dev = torch.device("cuda", 0)
+    w = synth.workload(args.profile, device=dev)
+    if args.heads != w.heads:
+        w = with_heads(w, args.heads)
+    kv = {"fp8": q.KV_FP8_E4M3, "nvfp4": q.KV_NVFP4, "fp8_per_token": q.KV_FP8_PER_TOKEN, "bf16": q.KV_BF16}[args.kv]
+    min_splits = 148 if w.batch == 1 else 0
+    pb = Problem(q, w, kv, min_splits=min_splits, algo=args.algo)
+    if kv == q.KV_BF16:
+        q.kv_pool_cast_bf16(w.pool_fp8, pb.data)
+    torch.cuda.empty_cache()
+    ms, att = time_problem(pb, args.steps, args.warmup)
+    pb.check(f"profile {args.profile}")
+    r = summarize(pb, ms, att, pk)
+    r.update({"workload": args.profile, "heads": w.heads, "kv": args.kv,
+              "algo": "tcgen05" if pb.plan.algo == 2 else "mma_sync", "kernel_digest": kernel_source_digest(
+                  "decode_tc.cu" if pb.plan.algo == 2 else "decode_mma.cu")})
+    print(json.dumps(r), flush=True)
 
 
 def extra_workloads(q, pk, dev, args, main_w=None):
@@ -600,6 +683,7 @@ def extra_workloads(q, pk, dev, args, main_w=None):
             base.step()
             dec_ev[k][1].record()
         torch.cuda.synchronize()
+        base.check("cast-then-attend BF16 decode")
         c_ms = float(np.mean([a.elapsed_time(b) for a, b in cast_ev]))
         d_ms = float(np.mean([a.elapsed_time(b) for a, b in dec_ev]))
         if best is None or c_ms + d_ms < best[0] + best[1]:
@@ -627,6 +711,7 @@ def extra_workloads(q, pk, dev, args, main_w=None):
             gb.step()
             e2.record()
         torch.cuda.synchronize()
+        gb.check("gather-then-cast BF16 decode")
         g_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in gev]))
         d_ms = float(np.mean([b.elapsed_time(c) for _, b, c in gev]))
         if gbest is None or g_ms + d_ms < gbest[0] + gbest[1]:

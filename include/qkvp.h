@@ -18,8 +18,9 @@
  *    pool to BF16 first (same page, section "SGLang implementation", item 3).
  *
  * Memory layout (all device buffers are caller-owned; the library allocates no device memory. Its
- * only global state is host-side: per device, four pinned staging buffers and events for the work
- * table upload of mla_decode_plan, and the fixed scratch of mla_decode_noalloc):
+ * only global state: per device, four pinned host staging buffers and events for the work table
+ * upload of mla_decode_plan, and the fixed device scratch array of mla_decode_noalloc with its
+ * static host table):
  *  - slot s = page * page_size + offset; page_size must be 64.
  *  - FP8 pool  : kv_data uint8 [num_pages][64][576], one E4M3 byte per latent element. The decode
  *                entry points read kv_data (any pool type) with 32-byte loads: it must be 32-byte aligned.
@@ -175,11 +176,14 @@ int kv_append_quant(const void* src, int32_t src_dtype, int64_t n_tokens,
  *  stream         stream of the table upload: an asynchronous copy from one of four library-owned
  *                 pinned buffers (per device, reused once its previous copy has completed), so the
  *                 call does not wait for earlier work on the stream and the host arrays may be
- *                 reused as soon as it returns. During stream capture, or if pinned memory is
- *                 refused, it copies from pageable memory instead.
+ *                 reused as soon as it returns. If pinned memory is refused it copies from
+ *                 pageable memory instead (staged by the runtime before the call returns).
  *
  * Returns QKVP_E_WORKSPACE (with plan->workspace_bytes filled) when workspace is non-NULL but
- * smaller than needed.
+ * smaller than needed, and QKVP_E_UNSUPPORTED when workspace is non-NULL and `stream` is being
+ * captured into a CUDA graph: the upload reads host memory that belongs to this call only, so a
+ * replayed graph would read it after it is gone. Plan outside capture; mla_decode_run,
+ * mla_decode_attend and mla_decode_combine only launch kernels and may be captured.
  */
 int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int32_t batch,
                     int32_t num_heads, int32_t page_size, int32_t kv_dtype, int32_t num_sms,
@@ -195,8 +199,11 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
  * where k_t is the dequantized latent without the global scale g (g = 1 for FP8 and BF16 pools;
  * "SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "SGLang implementation", item 3: the global
  * scale enters through the matrix-multiply scaling, not per element). The kernels dequantize in
- * registers, run Q.K^T and P.V on the tensor cores in BF16 with FP32 accumulation and an FP32
- * online softmax, write one partial per segment, and merge partials by log-sum-exp.
+ * registers and run Q.K^T and P.V on the tensor cores with FP16 operands and FP32 accumulation:
+ * every dequantized K/V value is exact in FP16, Q is converted from BF16 exactly (a row holding a
+ * value of 2^15 or more is first scaled by a power of two, folded into the logit scale), and the
+ * probabilities P keep 11 mantissa bits. The softmax runs online in FP32; each segment writes one
+ * partial, and partials are merged by log-sum-exp.
  *
  *  plan       from mla_decode_plan with the same kv_dtype, uploaded into this workspace.
  *  q          device bf16 [batch][num_heads][576].
@@ -241,10 +248,16 @@ int mla_decode_combine(const qkvp_plan* plan, float global_scale, void* out, flo
  * table plus partials above the array size (at 128 heads, about 250 split partials).
  *
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make this first call before any stream capture. Every call shares the one
- * array and leaves its partials there; calls whose GPU work overlaps (different streams or host
+ * that device current, and later calls on that device reuse it: a cudaDeviceReset between calls
+ * would leave that address stale, so do not reset a device between calls. Every call shares the
+ * one array and leaves its partials there; calls whose GPU work overlaps (different streams or host
  * threads) race on it, so the caller must serialise them. Nothing in the array needs to start at
  * zero: each call uploads its own table and writes every partial before reading it.
+ * The table is copied from static, pageable host memory, so the call returns only after the work
+ * already queued on `stream` has drained. It returns QKVP_E_UNSUPPORTED while `stream` is being
+ * captured into a CUDA graph (a replay would read a host table that later calls overwrite).
+ * It runs the mma.sync kernel family with the same split as mla_decode_plan for that family and
+ * the same SM count, so its output equals that of plan + run bit for bit.
  * Arguments as for mla_decode_plan and mla_decode_run (page size 64).
  */
 #define QKVP_NOALLOC_SCRATCH_BYTES (64ull << 20)

@@ -109,6 +109,16 @@ def _stream(stream):
     return torch.cuda.current_stream().cuda_stream
 
 
+def _table(kv_indptr, kv_len):
+    """The host page table as contiguous int32 arrays; kv_indptr must have len(kv_len) + 1 entries
+    (the library reads kv_indptr[r + 1] for every request r)."""
+    indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
+    lens = np.ascontiguousarray(kv_len, dtype=np.int32)
+    if indptr.ndim != 1 or lens.ndim != 1 or indptr.shape[0] != lens.shape[0] + 1:
+        raise ValueError(f"kv_indptr needs len(kv_len) + 1 = {lens.shape[0] + 1} entries, got {indptr.shape}")
+    return indptr, lens
+
+
 def _check(fn, status, raise_on_error):
     if status != QKVP_OK and raise_on_error:
         raise QkvpError(fn, status)
@@ -132,8 +142,7 @@ def mla_decode_plan(kv_indptr, kv_len, num_heads: int, kv_dtype: int, num_sms: i
                     min_splits: int = 0, algo: int = ALGO_AUTO, workspace=None,
                     page_size: int = PAGE_SIZE, stream=None, raise_on_error: bool = True):
     """Plan the split; with workspace=None only sizes are computed. Returns a qkvp_plan."""
-    indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
-    lens = np.ascontiguousarray(kv_len, dtype=np.int32)
+    indptr, lens = _table(kv_indptr, kv_len)
     plan = qkvp_plan()
     ws = _ptr(workspace)
     nbytes = int(workspace.numel() * workspace.element_size()) if workspace is not None else 0
@@ -184,8 +193,7 @@ def mla_decode_noalloc(kv_indptr, kv_len, num_heads: int, kv_dtype: int, q, kv_d
                        raise_on_error: bool = True) -> int:
     """Plan + decode with the library's fixed scratch array, for callers that cannot allocate
     device memory (see qkvp.h for the size limit and the sharing rules)."""
-    indptr = np.ascontiguousarray(kv_indptr, dtype=np.int32)
-    lens = np.ascontiguousarray(kv_len, dtype=np.int32)
+    indptr, lens = _table(kv_indptr, kv_len)
     st = load().mla_decode_noalloc(indptr.ctypes.data, lens.ctypes.data, int(lens.shape[0]), num_heads,
                                    kv_dtype, num_sms, min_splits, _ptr(q), _ptr(kv_data),
                                    _ptr(kv_scale), int(num_pages), _ptr(kv_indices), float(sm_scale),

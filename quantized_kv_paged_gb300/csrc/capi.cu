@@ -1,8 +1,8 @@
 // libqkvp C ABI: argument checks, the split-KV planner and kernel dispatch.
 //
-// Nothing here allocates device memory. mla_decode_plan stages its work table in a host vector
-// and copies it into the caller's workspace with one asynchronous copy on the caller's stream
-// (a pageable source is staged by the runtime before the call returns, so the vector may die).
+// Nothing here allocates device memory. mla_decode_plan builds its work table on the host (the
+// split itself is in split.cu) and copies it into the caller's workspace with one asynchronous copy
+// on the caller's stream, staged through library-owned pinned buffers.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -36,13 +36,12 @@ std::mutex g_stage_mutex;
 StageSlot g_stage[kStageDevices][kStageSlots];
 int g_stage_next[kStageDevices] = {};
 
-// Copies n bytes to the device buffer dst in stream order. Pinned staging where it can; a pageable
-// copy during stream capture (an event cannot be waited on there) or if pinned memory is refused.
+// Copies n bytes to the device buffer dst in stream order (never called during stream capture).
+// Pinned staging where it can; a pageable copy if pinned memory is refused (the runtime stages a
+// pageable source before the call returns, so `src` may be freed afterwards).
 cudaError_t upload_table(void* dst, const void* src, size_t n, cudaStream_t st) {
   int dev = -1;
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kStageDevices &&
-      cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone) {
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kStageDevices) {
     std::lock_guard<std::mutex> lock(g_stage_mutex);
     StageSlot& slot = g_stage[dev][g_stage_next[dev]];
     bool ok = true;
@@ -76,82 +75,6 @@ int query_sms() {
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
   return sms;
-}
-
-// Balanced split of the batch's pages over the workers.
-//
-// Requests are laid end to end in request order, one unit per page (ceil(len / 64) pages each),
-// and worker w takes the contiguous run of pages [w * quota, (w + 1) * quota), quota =
-// ceil(total / workers), so no worker holds more than one page above the mean. Each worker's run is
-// cut at request boundaries and into pieces of at most `cap` pages, cap = total / min_splits when a
-// minimum number of splits is asked for; each piece is one segment. Segments therefore come in
-// request order, and the segments of one request are contiguous.
-struct Split {
-  std::vector<Segment> segs;
-  std::vector<int32_t> wptr, rptr, wide;
-  int32_t split_reqs = 0, empty_reqs = 0, max_pages = 0, min_pages = 0, partials = 0, max_req_segs = 0;
-  int64_t total_pages = 0, total_tokens = 0;
-};
-
-void split_pages(const int32_t* indptr, const int32_t* len, int batch, int workers, int min_splits,
-                 Split& s) {
-  std::vector<int64_t> pages(batch), start(batch + 1, 0);
-  for (int r = 0; r < batch; ++r) {
-    pages[r] = (static_cast<int64_t>(len[r]) + kPage - 1) / kPage;
-    start[r + 1] = start[r] + pages[r];
-    s.total_tokens += len[r];
-  }
-  const int64_t total = start[batch];
-  s.total_pages = total;
-  const int64_t quota = total > 0 ? (total + workers - 1) / workers : 0;
-  int64_t cap = quota;
-  if (min_splits > 0 && total > 0) cap = std::max<int64_t>(1, std::min<int64_t>(quota, total / min_splits));
-  s.wptr.assign(workers + 1, 0);
-  s.max_pages = 0;
-  s.min_pages = total > 0 ? INT32_MAX : 0;
-  int r = 0;
-  for (int w = 0; w < workers; ++w) {
-    s.wptr[w] = static_cast<int32_t>(s.segs.size());
-    const int64_t a = std::min(total, w * quota), b = std::min(total, (w + 1) * quota);
-    s.max_pages = std::max<int32_t>(s.max_pages, static_cast<int32_t>(b - a));
-    if (total > 0) s.min_pages = std::min<int32_t>(s.min_pages, static_cast<int32_t>(b - a));
-    int64_t x = a;
-    while (x < b) {
-      while (r < batch && start[r + 1] <= x) ++r;
-      const int64_t y = std::min(b, start[r + 1]);
-      for (int64_t c = x; c < y; c += cap) {
-        const int64_t e = std::min(y, c + cap);
-        Segment g{};
-        g.req = r;
-        g.page_begin = static_cast<int32_t>(indptr[r] + (c - start[r]));
-        g.num_pages = static_cast<int32_t>(e - c);
-        const int64_t t0 = (c - start[r]) * kPage;
-        const int64_t t1 = std::min<int64_t>(len[r], (e - start[r]) * kPage);
-        g.num_tokens = static_cast<int32_t>(t1 - t0);
-        g.partial = 0;
-        s.segs.push_back(g);
-      }
-      x = y;
-    }
-  }
-  s.wptr[workers] = static_cast<int32_t>(s.segs.size());
-  // per-request segment ranges; requests with one segment write their output directly
-  s.rptr.assign(batch + 1, 0);
-  size_t k = 0;
-  int32_t part = 0;
-  for (int q = 0; q < batch; ++q) {
-    s.rptr[q] = static_cast<int32_t>(k);
-    size_t k0 = k;
-    while (k < s.segs.size() && s.segs[k].req == q) ++k;
-    const size_t n = k - k0;
-    if (n == 0) ++s.empty_reqs;
-    if (n >= 2) ++s.split_reqs;
-    s.max_req_segs = std::max<int32_t>(s.max_req_segs, static_cast<int32_t>(n));
-    if (n > static_cast<size_t>(kCombineWideSegs)) s.wide.push_back(q);
-    for (size_t i = k0; i < k; ++i) s.segs[i].partial = n == 1 ? -1 : part++;
-  }
-  s.rptr[batch] = static_cast<int32_t>(k);
-  s.partials = part;
 }
 
 bool finite_float(float x) { return std::isfinite(x); }
@@ -202,25 +125,14 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
                     qkvp_stream_t stream, qkvp_plan* plan) {
   if (!plan) return QKVP_E_INVALID;
   std::memset(plan, 0, sizeof(*plan));
-  if (batch < 0 || min_splits < 0) return QKVP_E_INVALID;
-  if (batch > 0 && (!kv_indptr_host || !kv_len_host)) return QKVP_E_INVALID;
-  if (page_size != QKVP_PAGE_SIZE) return QKVP_E_UNSUPPORTED;
-  if (num_heads < 16 || num_heads > 128 || num_heads % 16) return QKVP_E_UNSUPPORTED;
-  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16 &&
-      kv_dtype != QKVP_KV_FP8_PER_TOKEN)
-    return QKVP_E_UNSUPPORTED;
+  int st = check_plan_args(kv_indptr_host, kv_len_host, batch, num_heads, page_size, kv_dtype, min_splits);
+  if (st != QKVP_OK) return st;
   // The tcgen05 CTA-pair kernel always computes 128 head rows (fewer heads ride as zero rows), so it
   // costs the same at any head count; below 64 heads the mma.sync kernel, whose cost shrinks with
   // the heads, is faster (measured on the 44 x 32K FP8 workload: 16 heads 333 us, 32 heads 435 us,
   // 64 heads 653 us, against ~560 us for the tcgen05 kernel).
   if (algo == QKVP_ALGO_AUTO) algo = num_heads >= 64 ? QKVP_ALGO_TCGEN05 : QKVP_ALGO_MMA_SYNC;
   if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05) return QKVP_E_UNSUPPORTED;
-  if (batch > 0 && kv_indptr_host[0] != 0) return QKVP_E_INVALID;
-  for (int r = 0; r < batch; ++r) {
-    const int64_t np = static_cast<int64_t>(kv_indptr_host[r + 1]) - kv_indptr_host[r];
-    if (np < 0 || kv_len_host[r] < 0) return QKVP_E_INVALID;
-    if ((static_cast<int64_t>(kv_len_host[r]) + page_size - 1) / page_size > np) return QKVP_E_INVALID;
-  }
   int cpw, workers;
   if (algo == QKVP_ALGO_TCGEN05) {
     // one worker = one CTA pair; by default as many pairs as the device runs at once
@@ -242,31 +154,14 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
     workers = std::max(1, num_sms / cpw);
   }
 
-  Split s;
-  split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, s);
-  const TableLayout t = table_layout(static_cast<int64_t>(s.segs.size()), workers, batch);
-  plan->batch = batch;
-  plan->num_heads = num_heads;
-  plan->page_size = page_size;
-  plan->kv_dtype = kv_dtype;
-  plan->algo = algo;
-  plan->num_workers = workers;
-  plan->ctas_per_worker = cpw;
-  plan->num_segments = static_cast<int32_t>(s.segs.size());
-  plan->num_split_requests = s.split_reqs;
-  plan->num_empty_requests = s.empty_reqs;
-  plan->max_worker_pages = s.max_pages;
-  plan->min_worker_pages = s.min_pages;
-  plan->num_partials = s.partials;
-  plan->max_request_segments = s.max_req_segs;
-  plan->num_wide_requests = static_cast<int32_t>(s.wide.size());
-  plan->total_pages = s.total_pages;
-  plan->total_tokens = s.total_tokens;
-  plan->table_bytes = t.bytes;
-  plan->status_offset = t.status;
-  plan->partial_o_offset = t.bytes;
-  plan->partial_lse_offset = t.bytes + align_up(static_cast<uint64_t>(s.partials) * num_heads * QKVP_V_DIM * 4);
-  plan->workspace_bytes = plan->partial_lse_offset + align_up(static_cast<uint64_t>(s.partials) * num_heads * 4);
+  // count the segments, then fill the table arrays
+  SplitInfo info;
+  split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, SplitOut{}, info);
+  std::vector<Segment> segs(static_cast<size_t>(info.num_segments));
+  std::vector<int32_t> wptr(workers + 1), rptr(batch + 1), wide(batch > 0 ? batch : 1);
+  const SplitOut out{segs.data(), info.num_segments, wptr.data(), rptr.data(), wide.data()};
+  if (!split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, out, info)) return QKVP_E_INVALID;
+  fill_plan(plan, info, batch, num_heads, kv_dtype, algo, workers, cpw);
   if (workspace == nullptr) return QKVP_OK;  // size query: no device work
   if (workspace_bytes < plan->workspace_bytes || !aligned(workspace, kAlign)) {
     const uint64_t need = plan->workspace_bytes;
@@ -274,11 +169,16 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
     plan->workspace_bytes = need;
     return QKVP_E_WORKSPACE;
   }
-  std::vector<uint8_t> blob(t.bytes, 0);
-  if (!s.segs.empty()) std::memcpy(blob.data() + t.segs, s.segs.data(), s.segs.size() * sizeof(Segment));
-  std::memcpy(blob.data() + t.wptr, s.wptr.data(), s.wptr.size() * 4);
-  std::memcpy(blob.data() + t.rptr, s.rptr.data(), s.rptr.size() * 4);
-  if (!s.wide.empty()) std::memcpy(blob.data() + t.wide, s.wide.data(), s.wide.size() * 4);
+  // The table upload is a copy from host memory that this call owns only until it returns; a graph
+  // captured around it would read that memory again at every replay. Plans are made outside capture.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap) != cudaSuccess) return QKVP_E_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) {
+    std::memset(plan, 0, sizeof(*plan));
+    return QKVP_E_UNSUPPORTED;
+  }
+  std::vector<uint8_t> blob(plan->table_bytes);
+  write_table(blob.data(), out, info, workers, batch);
   cudaError_t e = upload_table(workspace, blob.data(), blob.size(), reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QKVP_E_CUDA;
   plan->magic = kPlanMagic;

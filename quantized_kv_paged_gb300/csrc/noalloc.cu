@@ -38,75 +38,6 @@ void* g_scratch_addr[kMaxDevices] = {};  // device address of g_scratch, per dev
 uint8_t g_table[kMaxSegments * sizeof(Segment) + (kMaxWorkers + 1) * 4 + (kMaxBatch + 1) * 4 + kMaxBatch * 4 +
                 4 * 256];
 
-// The same split as mla_decode_plan (requests end to end in page units, worker w takes pages
-// [w * quota, (w + 1) * quota), pieces cut at request boundaries and at `cap` pages), written
-// straight into static arrays. Returns the segment count, or -1 if it exceeds kMaxSegments.
-int64_t split_static(const int32_t* indptr, const int32_t* len, int batch, int workers, int min_splits,
-                     Segment* segs, int32_t* wptr, int32_t* rptr, int32_t* wide, qkvp_plan* plan) {
-  int64_t total = 0, tokens = 0;
-  for (int r = 0; r < batch; ++r) {
-    total += (static_cast<int64_t>(len[r]) + kPage - 1) / kPage;
-    tokens += len[r];
-  }
-  const int64_t quota = total > 0 ? (total + workers - 1) / workers : 0;
-  int64_t cap = quota;
-  if (min_splits > 0 && total > 0) cap = std::max<int64_t>(1, std::min<int64_t>(quota, total / min_splits));
-  int64_t n = 0, start_r = 0;
-  int r = 0;
-  int32_t max_pages = 0, min_pages = total > 0 ? INT32_MAX : 0;
-  for (int w = 0; w < workers; ++w) {
-    wptr[w] = static_cast<int32_t>(n);
-    const int64_t a = std::min(total, w * quota), b = std::min(total, (w + 1) * quota);
-    max_pages = std::max<int32_t>(max_pages, static_cast<int32_t>(b - a));
-    if (total > 0) min_pages = std::min<int32_t>(min_pages, static_cast<int32_t>(b - a));
-    int64_t x = a;
-    while (x < b) {
-      while (r < batch && start_r + (static_cast<int64_t>(len[r]) + kPage - 1) / kPage <= x) {
-        start_r += (static_cast<int64_t>(len[r]) + kPage - 1) / kPage;
-        ++r;
-      }
-      const int64_t end_r = start_r + (static_cast<int64_t>(len[r]) + kPage - 1) / kPage;
-      const int64_t y = std::min(b, end_r);
-      for (int64_t c = x; c < y; c += cap) {
-        if (n >= kMaxSegments) return -1;
-        const int64_t e = std::min(y, c + cap);
-        Segment g{};
-        g.req = r;
-        g.page_begin = static_cast<int32_t>(indptr[r] + (c - start_r));
-        g.num_pages = static_cast<int32_t>(e - c);
-        g.num_tokens = static_cast<int32_t>(std::min<int64_t>(len[r], (e - start_r) * kPage) - (c - start_r) * kPage);
-        segs[n++] = g;
-      }
-      x = y;
-    }
-  }
-  wptr[workers] = static_cast<int32_t>(n);
-  int64_t k = 0;
-  int32_t part = 0, split = 0, empty = 0, most = 0, nwide = 0;
-  for (int q = 0; q < batch; ++q) {
-    rptr[q] = static_cast<int32_t>(k);
-    const int64_t k0 = k;
-    while (k < n && segs[k].req == q) ++k;
-    if (k == k0) ++empty;
-    if (k - k0 >= 2) ++split;
-    most = std::max<int32_t>(most, static_cast<int32_t>(k - k0));
-    if (k - k0 > kCombineWideSegs) wide[nwide++] = q;
-    for (int64_t i = k0; i < k; ++i) segs[i].partial = (k - k0 == 1) ? -1 : part++;
-  }
-  rptr[batch] = static_cast<int32_t>(k);
-  plan->num_segments = static_cast<int32_t>(n);
-  plan->num_split_requests = split;
-  plan->num_empty_requests = empty;
-  plan->num_partials = part;
-  plan->max_request_segments = most;
-  plan->num_wide_requests = nwide;
-  plan->max_worker_pages = max_pages;
-  plan->min_worker_pages = min_pages;
-  plan->total_pages = total;
-  plan->total_tokens = tokens;
-  return n;
-}
-
 }  // namespace
 
 extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* kv_len_host, int32_t batch,
@@ -114,20 +45,10 @@ extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* 
                                   const void* q, const void* kv_data, const uint8_t* kv_scale,
                                   int64_t num_pages, const int32_t* kv_indices, float sm_scale,
                                   float global_scale, void* out, float* lse, qkvp_stream_t stream) {
-  // the same argument checks as mla_decode_plan, plus the fixed capacity of the scratch
-  if (batch < 0 || min_splits < 0) return QKVP_E_INVALID;
-  if (batch > 0 && (!kv_indptr_host || !kv_len_host)) return QKVP_E_INVALID;
-  if (num_heads < 16 || num_heads > 128 || num_heads % 16) return QKVP_E_UNSUPPORTED;
-  if (kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_NVFP4 && kv_dtype != QKVP_KV_BF16 &&
-      kv_dtype != QKVP_KV_FP8_PER_TOKEN)
-    return QKVP_E_UNSUPPORTED;
+  // the argument checks of mla_decode_plan, plus the fixed capacity of the scratch
   if (batch > kMaxBatch) return QKVP_E_WORKSPACE;
-  if (batch > 0 && kv_indptr_host[0] != 0) return QKVP_E_INVALID;
-  for (int r = 0; r < batch; ++r) {
-    const int64_t np = static_cast<int64_t>(kv_indptr_host[r + 1]) - kv_indptr_host[r];
-    if (np < 0 || kv_len_host[r] < 0) return QKVP_E_INVALID;
-    if ((static_cast<int64_t>(kv_len_host[r]) + kPage - 1) / kPage > np) return QKVP_E_INVALID;
-  }
+  int st = check_plan_args(kv_indptr_host, kv_len_host, batch, num_heads, kPage, kv_dtype, min_splits);
+  if (st != QKVP_OK) return st;
   int dev = 0;
   if (num_sms <= 0) {
     if (cudaGetDevice(&dev) != cudaSuccess) return QKVP_E_CUDA;
@@ -136,41 +57,30 @@ extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* 
   const int hc = mma_heads_per_cta(num_heads);
   if (hc == 0) return QKVP_E_UNSUPPORTED;
   const int cpw = num_heads / hc;
-  const int workers = std::min(kMaxWorkers, std::max(1, num_sms / cpw));
+  // the same worker count as mla_decode_plan for this kernel family (capped by the static arrays)
+  const int workers = std::max(1, num_sms / cpw);
+  if (workers > kMaxWorkers) return QKVP_E_WORKSPACE;
 
   std::lock_guard<std::mutex> lock(g_mutex);
-  // Lay the table out in static host storage exactly as mla_decode_run reads it. The segment count
-  // is bounded by kMaxSegments before the layout is known, so stage segments first, then place the
-  // worker and request ranges behind them.
+  // The planner of mla_decode_plan, writing into static storage: the same segments, in the same order.
   static Segment segs[kMaxSegments];
   static int32_t wptr[kMaxWorkers + 1];
   static int32_t rptr[kMaxBatch + 1];
   static int32_t wide[kMaxBatch];
+  const SplitOut table{segs, kMaxSegments, wptr, rptr, wide};
+  SplitInfo info;
+  if (!split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, table, info)) return QKVP_E_WORKSPACE;
   qkvp_plan plan;
   std::memset(&plan, 0, sizeof(plan));
-  const int64_t nseg = split_static(kv_indptr_host, kv_len_host, batch, workers, min_splits, segs, wptr, rptr, wide,
-                                    &plan);
-  if (nseg < 0) return QKVP_E_WORKSPACE;
-  const TableLayout t = table_layout(nseg, workers, batch);
-  plan.batch = batch;
-  plan.num_heads = num_heads;
-  plan.page_size = kPage;
-  plan.kv_dtype = kv_dtype;
-  plan.algo = QKVP_ALGO_MMA_SYNC;
-  plan.num_workers = workers;
-  plan.ctas_per_worker = cpw;
-  plan.table_bytes = t.bytes;
-  plan.status_offset = t.status;
-  plan.partial_o_offset = t.bytes;
-  plan.partial_lse_offset = t.bytes + align_up(static_cast<uint64_t>(plan.num_partials) * num_heads * kDv * 4);
-  plan.workspace_bytes = plan.partial_lse_offset + align_up(static_cast<uint64_t>(plan.num_partials) * num_heads * 4);
-  if (plan.workspace_bytes > kScratchBytes || t.bytes > sizeof(g_table)) return QKVP_E_WORKSPACE;
+  fill_plan(&plan, info, batch, num_heads, kv_dtype, QKVP_ALGO_MMA_SYNC, workers, cpw);
+  if (plan.workspace_bytes > kScratchBytes || plan.table_bytes > sizeof(g_table)) return QKVP_E_WORKSPACE;
   plan.magic = kPlanMagic;
-  std::memset(g_table, 0, t.bytes);
-  if (nseg > 0) std::memcpy(g_table + t.segs, segs, nseg * sizeof(Segment));
-  std::memcpy(g_table + t.wptr, wptr, (workers + 1) * 4);
-  std::memcpy(g_table + t.rptr, rptr, (batch + 1) * 4);
-  if (plan.num_wide_requests > 0) std::memcpy(g_table + t.wide, wide, plan.num_wide_requests * 4);
+  write_table(g_table, table, info, workers, batch);
+  // The table upload below reads g_table, which the next call overwrites: a captured graph would
+  // replay whatever the last call left there. The call is refused during capture.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap) != cudaSuccess) return QKVP_E_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return QKVP_E_UNSUPPORTED;
 
   // Set-up, once per device, with that device current: the device address of the scratch.
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QKVP_E_CUDA;
@@ -180,9 +90,9 @@ extern "C" int mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* 
     g_scratch_addr[dev] = p;
   }
   void* scratch = g_scratch_addr[dev];
-  // g_table is pageable: the runtime stages it before this call returns, so the next caller may
-  // overwrite it as soon as the lock is released.
-  if (cudaMemcpyAsync(scratch, g_table, t.bytes, cudaMemcpyHostToDevice,
+  // g_table is pageable: the runtime stages it before this call returns (after the stream's earlier
+  // work has drained), so the next caller may overwrite it as soon as the lock is released.
+  if (cudaMemcpyAsync(scratch, g_table, plan.table_bytes, cudaMemcpyHostToDevice,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return QKVP_E_CUDA;
   return mla_decode_run(&plan, q, kv_data, kv_scale, num_pages, kv_indices, sm_scale, global_scale, out,

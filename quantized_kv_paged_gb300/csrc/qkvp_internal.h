@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include "../../include/qkvp.h"
+
 namespace qkvp {
 
 constexpr int kLatent = 576;            // 512 nope + 64 rope
@@ -81,6 +83,35 @@ inline TableLayout table_layout(int64_t segments, int64_t workers, int64_t batch
   t.bytes = t.status + kTableAlign;
   return t;
 }
+
+// The split-KV planner (split.cu), shared by mla_decode_plan and mla_decode_noalloc. It writes into
+// the caller's arrays: segs [max_segs], wptr [workers + 1], rptr [batch + 1], wide [batch]. With
+// segs == nullptr it only counts (num_segments, page totals and per-worker page counts); the
+// per-request fields of SplitInfo need the segments. Returns false when more than max_segs
+// segments would be written.
+struct SplitOut {
+  Segment* segs = nullptr;
+  int64_t max_segs = 0;
+  int32_t* wptr = nullptr;
+  int32_t* rptr = nullptr;
+  int32_t* wide = nullptr;
+};
+struct SplitInfo {
+  int64_t num_segments = 0;
+  int32_t split_reqs = 0, empty_reqs = 0, max_pages = 0, min_pages = 0, partials = 0, max_req_segs = 0,
+          num_wide = 0;
+  int64_t total_pages = 0, total_tokens = 0;
+};
+bool split_pages(const int32_t* indptr, const int32_t* len, int batch, int workers, int min_splits,
+                 const SplitOut& out, SplitInfo& info);
+// The argument checks of mla_decode_plan that need no device (status code, QKVP_OK if they pass).
+int check_plan_args(const int32_t* indptr, const int32_t* len, int batch, int num_heads, int page_size,
+                    int kv_dtype, int min_splits);
+// Sets every field of *plan except magic from a split (table layout, offsets and workspace size).
+void fill_plan(qkvp_plan* plan, const SplitInfo& info, int batch, int num_heads, int kv_dtype, int algo,
+               int workers, int ctas_per_worker);
+// Writes the work table of a filled split into blob [table_layout(...).bytes], zeros elsewhere.
+void write_table(uint8_t* blob, const SplitOut& s, const SplitInfo& info, int workers, int batch);
 
 // Arguments of the extend-path gather (kv_gather_fp8).
 struct GatherArgs {

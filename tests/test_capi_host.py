@@ -178,3 +178,15 @@ def test_gather_entry_points_reject_before_launch(lib):
     assert g(16, 64, 10, 16, 0, 16, None) == q.QKVP_OK
     assert g(None, 64, 10, 16, 3, 16, None) == q.QKVP_E_INVALID
     assert g(16, 64, 10, 16, 3, 8, None) == q.QKVP_E_INVALID
+
+
+def test_binding_refuses_a_short_or_long_indptr(lib):
+    """The C side reads kv_indptr[r + 1] for every request r: the binding checks the length first."""
+    lens = np.array([100, 5], np.int32)
+    for bad in (np.array([0, 2], np.int32), np.array([0, 2, 3, 4], np.int32)):
+        with pytest.raises(ValueError):
+            q.mla_decode_plan(bad, lens, 16, q.KV_FP8_E4M3, num_sms=4)
+        with pytest.raises(ValueError):
+            q.mla_decode_noalloc(bad, lens, 16, q.KV_FP8_E4M3, 16, 16, None, 4, 16, 0.1, 1.0, 16, None,
+                                 num_sms=4, stream=0)
+    assert plan(np.array([0, 2, 3], np.int32), lens, heads=16, sms=4).status == q.QKVP_OK

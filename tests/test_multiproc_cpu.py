@@ -47,6 +47,10 @@ def test_two_ranks_agree_on_the_slowest_time():
             p.start()
         for p in procs:
             p.join(timeout=120)
+        for p in procs:                      # a hung rank must not outlive the test
+            if p.is_alive():
+                p.terminate()
+                p.join(timeout=10)
         codes = [p.exitcode for p in procs]
         assert codes == [0, 0], codes
         assert dict(out) == {0: 2.5, 1: 2.5}
