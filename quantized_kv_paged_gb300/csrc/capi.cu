@@ -157,7 +157,8 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   // count the segments, then fill the table arrays
   SplitInfo info;
   split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, SplitOut{}, info);
-  std::vector<Segment> segs(static_cast<size_t>(info.num_segments));
+  // at least one element, so that the fill pass gets a non-null array even without segments
+  std::vector<Segment> segs(static_cast<size_t>(std::max<int64_t>(1, info.num_segments)));
   std::vector<int32_t> wptr(workers + 1), rptr(batch + 1), wide(batch > 0 ? batch : 1);
   const SplitOut out{segs.data(), info.num_segments, wptr.data(), rptr.data(), wide.data()};
   if (!split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, out, info)) return QKVP_E_INVALID;

@@ -190,3 +190,10 @@ def test_binding_refuses_a_short_or_long_indptr(lib):
             q.mla_decode_noalloc(bad, lens, 16, q.KV_FP8_E4M3, 16, 16, None, 4, 16, 0.1, 1.0, 16, None,
                                  num_sms=4, stream=0)
     assert plan(np.array([0, 2, 3], np.int32), lens, heads=16, sms=4).status == q.QKVP_OK
+
+
+def test_plan_of_only_empty_requests(lib):
+    """No segments at all: the plan still lists the empty requests (the combine writes their zeros)."""
+    p = plan(np.array([0, 1, 1], np.int32), np.array([0, 0], np.int32), heads=16, sms=4)
+    assert p.status == q.QKVP_OK and p.num_segments == 0 and p.num_empty_requests == 2
+    assert p.total_pages == 0 and p.num_partials == 0
