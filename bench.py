@@ -524,6 +524,9 @@ def main():
                          "and print a short summary instead of the benchmark line")
     ap.add_argument("--kv", default="fp8", choices=["fp8", "nvfp4", "fp8_per_token", "bf16"],
                     help="pool type of the --profile workload")
+    ap.add_argument("--op", default="decode", choices=["decode", "gather", "cast"],
+                    help="what --profile times: the decode step, the extend-path gather into the FP8 "
+                         "workspace, or the pool-wide cast to BF16")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.profile:
@@ -611,6 +614,32 @@ def profile_main(args):
     if args.heads != w.heads:
         w = with_heads(w, args.heads)
     kv = {"fp8": q.KV_FP8_E4M3, "nvfp4": q.KV_NVFP4, "fp8_per_token": q.KV_FP8_PER_TOKEN, "bf16": q.KV_BF16}[args.kv]
+    if args.op == "gather":
+        if kv == q.KV_NVFP4:
+            nv = Problem(q, w, kv)
+            data, scale = nv.data, nv.scale
+        else:
+            data, scale = w.pool_fp8, None
+        r = extend_gather(q, pk, w, kv, data, scale, 1.0, args.steps, args.warmup)
+        r.update({"workload": args.profile, "kv": args.kv, "op": "gather"})
+        print(json.dumps(r), flush=True)
+        return
+    if args.op == "cast":
+        out = torch.empty((w.num_pages, 64, LATENT), dtype=torch.int16, device=dev)
+        for _ in range(args.warmup):
+            q.kv_pool_cast_bf16(w.pool_fp8, out)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            q.kv_pool_cast_bf16(w.pool_fp8, out)
+            b.record()
+        torch.cuda.synchronize()
+        ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+        moved = 3 * w.num_pages * 64 * LATENT
+        print(json.dumps({"workload": args.profile, "op": "cast", "us": round(ms * 1e3, 2), "bytes_moved": moved,
+                          "gbs": round(moved / (ms * 1e-3) / 1e9, 1)}), flush=True)
+        return
     min_splits = 148 if w.batch == 1 else 0
     pb = Problem(q, w, kv, min_splits=min_splits, algo=args.algo)
     if kv == q.KV_BF16:
