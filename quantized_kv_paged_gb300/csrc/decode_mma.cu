@@ -214,27 +214,21 @@ __device__ __forceinline__ void dequant_page(const uint8_t* s_raw, uint8_t* s_kv
     for (int row = tid; row < kPage; row += NT)
       *reinterpret_cast<float*>(s_kv + row * kRowBytes + kSigByte) = row < valid ? s_sc[row] : 0.0f;
   } else if (KV == KV_NVFP4) {
+    // one 4-byte word (8 codes, inside one 16-element block) per thread and one 16-byte store: the
+    // lanes of a warp write consecutive 16-byte chunks, so the stores are free of bank conflicts
+    // (64-byte chunks per thread, stored in order, hit 4-way conflicts that bound this path)
     const uint8_t* s_sc = s_raw + kPage * kPacked;
-    for (int c = tid; c < valid * (kPacked / 16); c += NT) {
-      const int row = c / (kPacked / 16), ch = c % (kPacked / 16);
-      const uint4 v = *reinterpret_cast<const uint4*>(s_raw + c * 16);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      const uint32_t sa = s_sc[row * kScales + 2 * ch], sb = s_sc[row * kScales + 2 * ch + 1];
-      const uint32_t ha = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sa | (sa << 8)));
-      const uint32_t hb = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
-      uint32_t o[16];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t c4[4];
-        dev::e2m1x8_to_f16x2x4(w[k], c4);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) o[4 * k + b] = dev::hmul2_f16(c4[b], k < 2 ? ha : hb);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(s_kv + row * kRowBytes + ch * 64);
-      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-      dst[2] = make_uint4(o[8], o[9], o[10], o[11]);
-      dst[3] = make_uint4(o[12], o[13], o[14], o[15]);
+    constexpr int kWords = kPacked / 4;               // 72 words per row
+    for (int c = tid; c < valid * kWords; c += NT) {
+      const int row = c / kWords, w = c % kWords;
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(s_raw + row * kPacked + 4 * w);
+      const uint32_t sb = s_sc[row * kScales + (w >> 1)];
+      const uint32_t hs = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(sb | (sb << 8)));
+      uint32_t c4[4];
+      dev::e2m1x8_to_f16x2x4(v, c4);
+      *reinterpret_cast<uint4*>(s_kv + row * kRowBytes + w * 16) =
+          make_uint4(dev::hmul2_f16(c4[0], hs), dev::hmul2_f16(c4[1], hs), dev::hmul2_f16(c4[2], hs),
+                     dev::hmul2_f16(c4[3], hs));
     }
   } else {
     // BF16 pool: the rows were copied in as BF16; convert them to FP16 in place

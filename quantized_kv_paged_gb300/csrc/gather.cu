@@ -32,69 +32,73 @@ __device__ __forceinline__ int find_request(const int64_t* tok_indptr, int batch
 __device__ __forceinline__ float f16_low(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))); }
 __device__ __forceinline__ float f16_high(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))); }
 
+// Two E4M3 pairs (16-bit results of the pair conversions) -> one word, first pair in the low half.
+__device__ __forceinline__ uint32_t pack_b16x2(uint32_t lo, uint32_t hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l, h;\n\tcvt.u16.u32 l, %1;\n\tcvt.u16.u32 h, %2;\n\tmov.b32 %0, {l, h};\n\t}"
+      : "=r"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
 // One NVFP4 block (16 elements: 8 packed bytes, one scale byte) -> 16 E4M3 bytes.
 __device__ __forceinline__ uint4 nvfp4_block_to_e4m3(uint2 d, uint32_t s8, float g) {
-  const uint32_t w[2] = {d.x, d.y};
-  uint32_t bytes[4] = {0, 0, 0, 0};
-  if ((s8 & 0x7Fu) == 0x7Fu) {                // NaN block scale: every element is NaN -> 0x7F
-    bytes[0] = bytes[1] = bytes[2] = bytes[3] = 0x7F7F7F7Fu;
-  } else if (g == 1.0f) {
+  if ((s8 & 0x7Fu) == 0x7Fu)                  // NaN block scale: every element is NaN -> 0x7F
+    return make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const uint32_t s2 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(s8 | (s8 << 8)));
+  uint32_t c[8];                              // code pairs from byte registers; pair k = elements 2k, 2k + 1
+  dev::e2m1x8_to_f16x2x4(d.x, *reinterpret_cast<uint32_t(*)[4]>(c));
+  dev::e2m1x8_to_f16x2x4(d.y, *reinterpret_cast<uint32_t(*)[4]>(c + 4));
+  uint32_t e[8];
+  if (g == 1.0f) {
     // s * e has at most 6 significant bits within [2^-10, 2688]: exact in FP16, so one FP16x2
     // multiply and one FP16x2 -> E4M3x2 conversion (RNE, satfinite) per pair
-    const uint32_t s2 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(s8 | (s8 << 8)));
-    uint32_t c0[4], c1[4];                    // code pairs from byte registers
-    dev::e2m1x8_to_f16x2x4(w[0], c0);
-    dev::e2m1x8_to_f16x2x4(w[1], c1);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t v2 = dev::hmul2_f16(k < 4 ? c0[k] : c1[k - 4], s2);
-      bytes[k >> 1] |= dev::f16x2_to_e4m3x2(v2) << (16 * (k & 1));
-    }
+    for (int k = 0; k < 8; ++k) e[k] = dev::f16x2_to_e4m3x2(dev::hmul2_f16(c[k], s2));
   } else {
     // the exact product in FP16x2, widened to FP32, one FP32 multiply by g per element, one
     // conversion per pair (RNE, satfinite; no NaN can reach it: NaN scales were handled above)
-    const uint32_t s2 = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(s8 | (s8 << 8)));
-    uint32_t c0[4], c1[4];                    // packed byte k: elements 2k (low nibble), 2k + 1
-    dev::e2m1x8_to_f16x2x4(w[0], c0);
-    dev::e2m1x8_to_f16x2x4(w[1], c1);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t v2 = dev::hmul2_f16(k < 4 ? c0[k] : c1[k - 4], s2);
-      const float v0 = __fmul_rn(f16_low(v2), g), v1 = __fmul_rn(f16_high(v2), g);
-      bytes[k >> 1] |= dev::f32x2_to_e4m3x2(v0, v1) << (16 * (k & 1));
+      const uint32_t v2 = dev::hmul2_f16(c[k], s2);
+      e[k] = dev::f32x2_to_e4m3x2(__fmul_rn(f16_low(v2), g), __fmul_rn(f16_high(v2), g));
     }
   }
-  return make_uint4(bytes[0], bytes[1], bytes[2], bytes[3]);
+  return make_uint4(pack_b16x2(e[0], e[1]), pack_b16x2(e[2], e[3]), pack_b16x2(e[4], e[5]), pack_b16x2(e[6], e[7]));
 }
 
-// Each CTA pass covers 64 workspace rows; thread (sub, blk) handles block blk of rows
-// base + sub + 8k, k = 0..7, in three phases so that the eight dependent lookup chains and the eight
-// data loads are all in flight together: table lookups, loads, then conversion and stores.
+// Each CTA pass covers 64 workspace rows. The 64 rows' pool slots are resolved once per pass (one
+// thread per row: the request by binary search over tok_indptr, then the page-table entry, every
+// entry bounds-checked) into shared memory; thread (sub, blk) then handles block blk of rows
+// base + sub + 8k, k = 0..7, with its eight loads in flight together before any conversion.
 template <int KV>
 __global__ void __launch_bounds__(kGatherThreads) gather_fp8_kernel(const GatherArgs a) {
   constexpr int kRows = 8;
+  constexpr int kPassRows = kRowsPerPass * kRows;
+  __shared__ int64_t s_slot[kPassRows];
   const int sub = threadIdx.x / 36, blk = threadIdx.x % 36;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kRowsPerPass * kRows; base < a.total_tokens;
-       base += static_cast<int64_t>(gridDim.x) * kRowsPerPass * kRows) {
-    int64_t slot[kRows];
-    int r = find_request(a.tok_indptr, a.batch, base + sub);
-#pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      const int64_t row = base + sub + kRowsPerPass * k;
-      slot[k] = -1;
-      if (row >= a.total_tokens) continue;
-      while (r + 1 < a.batch && a.tok_indptr[r + 1] <= row) ++r;
-      const int64_t t = row - a.tok_indptr[r];
-      const int64_t p = a.kv_indptr[r] + t / kPage;
-      if (t >= 0 && p >= 0 && p < a.kv_indptr[r + 1] && p < a.nnz) {
-        const int64_t page = a.kv_indices[p];
-        if (page >= 0 && page < a.num_pages) slot[k] = page * kPage + t % kPage;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kPassRows; base < a.total_tokens;
+       base += static_cast<int64_t>(gridDim.x) * kPassRows) {
+    if (threadIdx.x < kPassRows) {
+      const int64_t row = base + threadIdx.x;
+      int64_t slot = -1;
+      if (row < a.total_tokens) {
+        const int r = find_request(a.tok_indptr, a.batch, row);
+        const int64_t t = row - a.tok_indptr[r];
+        const int64_t p = a.kv_indptr[r] + t / kPage;
+        if (t >= 0 && p >= 0 && p < a.kv_indptr[r + 1] && p < a.nnz) {
+          const int64_t page = a.kv_indices[p];
+          if (page >= 0 && page < a.num_pages) slot = page * kPage + t % kPage;
+        }
       }
+      s_slot[threadIdx.x] = slot;
     }
+    __syncthreads();
+    int64_t slot[kRows];
     uint4 raw[kRows];
     uint32_t s8[kRows];
 #pragma unroll
     for (int k = 0; k < kRows; ++k) {
+      slot[k] = s_slot[sub + kRowsPerPass * k];
       raw[k] = make_uint4(0, 0, 0, 0);
       s8[k] = 0;
       if (slot[k] < 0) continue;
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_fp8_kernel(const Gather
         s8[k] = a.kv_scale[slot[k] * kScales + blk];
       }
     }
+    __syncthreads();                          // s_slot is rewritten by the next pass
 #pragma unroll
     for (int k = 0; k < kRows; ++k) {
       const int64_t row = base + sub + kRowsPerPass * k;
@@ -154,7 +159,7 @@ cudaError_t launch_gather_fp8(const GatherArgs& a, cudaStream_t s) {
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (a.total_tokens + kRowsPerPass * 8 - 1) / (kRowsPerPass * 8);
+  const int64_t want = (a.total_tokens + kRowsPerPass * 8 - 1) / (kRowsPerPass * 8);   // passes of 64 rows
   const int64_t cap = static_cast<int64_t>(sms > 0 ? sms : 148) * 8;      // 8 CTAs of 288 threads per SM
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   if (a.kv_dtype == KV_FP8) gather_fp8_kernel<KV_FP8><<<grid, kGatherThreads, 0, s>>>(a);

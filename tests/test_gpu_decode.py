@@ -159,7 +159,9 @@ def _full_check(name, kv, g_mode="one", n_pairs=12, append=False, algo=0):
     min_splits = 148 if w.batch == 1 else 0
     out, lse, plan = gpu_decode(w, kv, pools, g, min_splits=min_splits, lens=lens, algo=algo)
     assert torch.all(torch.isfinite(out.float())) and torch.all(torch.isfinite(lse))
-    pairs = _sample_pairs(w, n_pairs, 7)
+    # n_pairs None: every (request, head) output of the step
+    pairs = _sample_pairs(w, n_pairs, 7) if n_pairs else np.array(
+        [[r, h] for r in range(w.batch) for h in range(w.heads)], np.int32)
     o_ref, lse_ref = oracle_decode(w, kv, host, g, pairs=pairs, lens=lens)
     got = out.float().cpu().numpy()[pairs[:, 0], pairs[:, 1]]
     gl = lse.cpu().numpy()[pairs[:, 0], pairs[:, 1]]
