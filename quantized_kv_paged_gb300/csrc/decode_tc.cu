@@ -777,17 +777,16 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       store_row();
     }
     l += lsum;
+    // each warp hands its own 32 rows (2 KB, contiguous in the 64-byte swizzle) to the peer as soon as
+    // they are written: no CTA-wide wait before the copies. P_FULL(s) completes with the four local
+    // warps' arrivals and the peer's four 2 KB copies.
     tc::fence_proxy_async_smem();
-    tc::mbar_arrive(sy.bar(B_P_LOCAL + s));
-    bool ok = true;
-    if (h == 0) {
-      ok = sy.wait(B_P_LOCAL + s, (g >> 1) & 1, false, 8192);
-      if (ok) {
-        tc::bulk_copy_to_peer(prow, prow, kPHalf, sy.bar(B_P_FULL + s), peer);
-        tc::mbar_arrive_expect_tx(sy.bar(B_P_FULL + s), kPHalf);   // completes with the peer's half
-      }
+    __syncwarp();
+    if ((h & 31) == 0) {
+      const uint32_t wrows = pbuf + s * kPBytes + c * kPHalf + (h >> 5) * (kPHalf / 4);
+      tc::bulk_copy_to_peer(wrows, wrows, kPHalf / 4, sy.bar(B_P_FULL + s), peer);
+      tc::mbar_arrive_expect_tx(sy.bar(B_P_FULL + s), kPHalf / 4);
     }
-    if (!__all_sync(0xffffffffu, ok)) return;
     cur = nx;
     pg = npg;
     if (!last) continue;
@@ -858,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
       tc::mbar_init(sy.bar(B_S_FULL + i), 1);
       tc::mbar_init(sy.bar(B_S_FREE + i), 128);
       tc::mbar_init(sy.bar(B_P_LOCAL + i), 128);
-      tc::mbar_init(sy.bar(B_P_FULL + i), 1);        // plus the peer's 8 KB of P, counted in bytes
+      tc::mbar_init(sy.bar(B_P_FULL + i), 4);        // one per softmax warp, plus the peer's 8 KB of P in bytes
       tc::mbar_init(sy.bar(B_P_FREE + i), 2);        // P.V of the page in both CTAs
       tc::mbar_init(sy.bar(B_O_DONE + i), 1);
       tc::mbar_init(sy.bar(B_RM_FULL + i), 1);       // plus the peer's 128 x 4 bytes, counted in bytes
