@@ -17,6 +17,7 @@ using namespace qkvp;
 namespace {
 
 constexpr uint64_t kAlign = kTableAlign;
+constexpr int kTcSegmentCost = 14;  // pages of work one request start costs the tcgen05 kernel
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -154,14 +155,21 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
     workers = std::max(1, num_sms / cpw);
   }
 
+  // The tcgen05 kernel pays for every request a CTA pair starts: the request's Q is loaded (about
+  // 11 us) and the pipeline drains and refills around it (measured with a segment timeline of the
+  // kernel on one GB300, at ~1.6 us per page in steady state). Its split balances pages plus this
+  // many pages per request started (14 measured best among 0, 8, 14, 20, 28: mixed batch 234 ->
+  // 192 us, 44 x 32K 515 -> 509 us, NVFP4 10 x 160K 568 -> 550 us); the mma.sync kernel's split
+  // gives equal page quotas.
+  const int seg_cost = algo == QKVP_ALGO_TCGEN05 ? kTcSegmentCost : 0;
   // count the segments, then fill the table arrays
   SplitInfo info;
-  split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, SplitOut{}, info);
+  split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, SplitOut{}, info, seg_cost);
   // at least one element, so that the fill pass gets a non-null array even without segments
   std::vector<Segment> segs(static_cast<size_t>(std::max<int64_t>(1, info.num_segments)));
   std::vector<int32_t> wptr(workers + 1), rptr(batch + 1), wide(batch > 0 ? batch : 1);
   const SplitOut out{segs.data(), info.num_segments, wptr.data(), rptr.data(), wide.data()};
-  if (!split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, out, info)) return QKVP_E_INVALID;
+  if (!split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, out, info, seg_cost)) return QKVP_E_INVALID;
   fill_plan(plan, info, batch, num_heads, kv_dtype, algo, workers, cpw);
   if (workspace == nullptr) return QKVP_OK;  // size query: no device work
   if (workspace_bytes < plan->workspace_bytes || !aligned(workspace, kAlign)) {

@@ -102,8 +102,10 @@ struct SplitInfo {
           num_wide = 0;
   int64_t total_pages = 0, total_tokens = 0;
 };
+// seg_cost > 0 balances pages + seg_cost per request each worker starts (the tcgen05 kernel loads a
+// new request's Q and refills its pipeline at each); 0 gives every worker an equal page quota.
 bool split_pages(const int32_t* indptr, const int32_t* len, int batch, int workers, int min_splits,
-                 const SplitOut& out, SplitInfo& info);
+                 const SplitOut& out, SplitInfo& info, int seg_cost = 0);
 // The argument checks of mla_decode_plan that need no device (status code, QKVP_OK if they pass).
 int check_plan_args(const int32_t* indptr, const int32_t* len, int batch, int num_heads, int page_size,
                     int kv_dtype, int min_splits);

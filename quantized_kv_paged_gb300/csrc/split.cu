@@ -72,7 +72,7 @@ void write_table(uint8_t* blob, const SplitOut& s, const SplitInfo& info, int wo
 }
 
 bool split_pages(const int32_t* indptr, const int32_t* len, int batch, int workers, int min_splits,
-                 const SplitOut& out, SplitInfo& info) {
+                 const SplitOut& out, SplitInfo& info, int seg_cost) {
   info = SplitInfo{};
   auto pages_of = [len](int r) { return (static_cast<int64_t>(len[r]) + kPage - 1) / kPage; };
   int64_t total = 0;
@@ -84,13 +84,64 @@ bool split_pages(const int32_t* indptr, const int32_t* len, int batch, int worke
   const int64_t quota = total > 0 ? (total + workers - 1) / workers : 0;
   int64_t cap = quota;
   if (min_splits > 0 && total > 0) cap = std::max<int64_t>(1, std::min<int64_t>(quota, total / min_splits));
+
+  // Worker page ranges. With seg_cost = 0, equal quotas. Otherwise every request a worker starts costs
+  // seg_cost pages on top of its pages, and each worker fills up to a budget in request order; the
+  // budget is the smallest for which `workers` workers cover every page (bisection). Walks the
+  // requests from `x` (in request `r`, whose first page unit is `start_r`) and returns the end of
+  // one worker's range.
+  auto fill = [&](int64_t budget, int64_t x, int& r, int64_t& start_r) {
+    int64_t cost = 0;
+    while (x < total) {
+      while (r < batch && start_r + pages_of(r) <= x) {
+        start_r += pages_of(r);
+        ++r;
+      }
+      const int64_t room = budget - cost - seg_cost;
+      if (room <= 0) break;
+      const int64_t take = std::min(room, start_r + pages_of(r) - x);
+      cost += seg_cost + take;
+      x += take;
+      if (x < start_r + pages_of(r)) break;   // the budget ended inside this request
+    }
+    return x;
+  };
+  int64_t budget = quota;
+  if (seg_cost > 0 && total > 0) {
+    auto covers = [&](int64_t bgt) {
+      int64_t x = 0, start_r = 0;
+      int r = 0;
+      for (int w = 0; w < workers && x < total; ++w) x = fill(bgt, x, r, start_r);
+      return x >= total;
+    };
+    int64_t lo = quota, hi = quota + static_cast<int64_t>(seg_cost) * (batch + 1) + 1;
+    while (!covers(hi)) hi *= 2;
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (covers(mid)) hi = mid; else lo = mid + 1;
+    }
+    budget = lo;
+    // ranges may exceed the equal quota now: cut them only for a requested minimum of splits
+    cap = min_splits > 0 ? std::max<int64_t>(1, std::min<int64_t>(budget, total / min_splits)) : total;
+  }
+
   info.max_pages = 0;
   info.min_pages = total > 0 ? INT32_MAX : 0;
   int64_t n = 0, start_r = 0;   // segments so far; first page unit of request r
   int r = 0;
+  int64_t fx = 0, fstart_r = 0;
+  int fr = 0;
   for (int w = 0; w < workers; ++w) {
     if (out.wptr) out.wptr[w] = static_cast<int32_t>(n);
-    const int64_t a = std::min(total, w * quota), b = std::min(total, (w + 1) * quota);
+    int64_t a, b;
+    if (seg_cost > 0) {
+      a = fx;
+      b = fill(budget, fx, fr, fstart_r);
+      fx = b;
+    } else {
+      a = std::min(total, w * quota);
+      b = std::min(total, (w + 1) * quota);
+    }
     info.max_pages = std::max<int32_t>(info.max_pages, static_cast<int32_t>(b - a));
     if (total > 0) info.min_pages = std::min<int32_t>(info.min_pages, static_cast<int32_t>(b - a));
     int64_t x = a;

@@ -75,7 +75,7 @@ def test_plan_workspace_too_small_reports_size(lib):
 def test_split_is_balanced_and_covers_every_page(lib):
     lens = np.array([32768] * 44, np.int32)
     ptr = np.concatenate([[0], np.cumsum((lens + 63) // 64)]).astype(np.int32)
-    p = plan(ptr, lens)
+    p = plan(ptr, lens, algo=q.ALGO_MMA_SYNC)   # 76 workers of two 64-head CTAs, equal page quotas
     assert p.total_pages == 44 * 512 and p.total_tokens == 44 * 32768
     assert p.ctas_per_worker * p.num_workers <= 152
     # makespan is the ceiling of the mean: no worker holds more than one page above it
@@ -197,3 +197,33 @@ def test_plan_of_only_empty_requests(lib):
     p = plan(np.array([0, 1, 1], np.int32), np.array([0, 0], np.int32), heads=16, sms=4)
     assert p.status == q.QKVP_OK and p.num_segments == 0 and p.num_empty_requests == 2
     assert p.total_pages == 0 and p.num_partials == 0
+
+
+def test_tcgen05_split_charges_request_starts(lib):
+    """The tcgen05 plan balances pages plus a fixed cost per request a CTA pair starts (its Q load and
+    pipeline refill): pairs that start two requests get fewer pages than pairs that start one, and no
+    more requests are cut than under equal page quotas."""
+    lens = np.array([32768] * 44, np.int32)
+    ptr = np.concatenate([[0], np.cumsum((lens + 63) // 64)]).astype(np.int32)
+    tc = plan(ptr, lens, algo=q.ALGO_TCGEN05)
+    eq = plan(ptr, lens, algo=q.ALGO_MMA_SYNC)
+    assert tc.num_workers == eq.num_workers == 76 and tc.ctas_per_worker == 2
+    assert tc.total_pages == eq.total_pages == 44 * 512
+    assert tc.num_segments <= eq.num_segments
+    mean = -(-tc.total_pages // tc.num_workers)
+    assert tc.min_worker_pages < mean <= tc.max_worker_pages          # uneven on purpose
+    assert tc.max_worker_pages - tc.min_worker_pages <= 14            # one request start apart
+    # a mixed batch: no more request starts than under equal quotas
+    rng = np.random.default_rng(0)
+    ml = np.exp(rng.uniform(np.log(512), np.log(65536), 64)).astype(np.int32)
+    mp = np.concatenate([[0], np.cumsum((ml + 63) // 64)]).astype(np.int32)
+    a, b = plan(mp, ml, algo=q.ALGO_TCGEN05), plan(mp, ml, algo=q.ALGO_MMA_SYNC)
+    assert a.total_pages == b.total_pages and a.num_segments <= b.num_segments
+    # 70 requests of 100 pages over 76 pairs: equal quotas of 93 pages cut 69 requests (two request
+    # starts, 93 + 2 x 14 = 121 pages of cost); one whole request per pair costs 100 + 14 = 114, so
+    # the budgeted split cuts none and leaves six pairs idle
+    sl = np.array([6400] * 70, np.int32)
+    sp = np.concatenate([[0], np.cumsum((sl + 63) // 64)]).astype(np.int32)
+    a, b = plan(sp, sl, algo=q.ALGO_TCGEN05), plan(sp, sl, algo=q.ALGO_MMA_SYNC)
+    assert b.num_segments == 145 and b.max_worker_pages == 93
+    assert a.num_segments == 70 and a.max_worker_pages == 100 and a.min_worker_pages == 0
