@@ -159,9 +159,11 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   // 11 us) and the pipeline drains and refills around it (measured with a segment timeline of the
   // kernel on one GB300, at ~1.6 us per page in steady state). Its split balances pages plus this
   // many pages per request started (14 measured best among 0, 8, 14, 20, 28: mixed batch 234 ->
-  // 192 us, 44 x 32K 515 -> 509 us, NVFP4 10 x 160K 568 -> 550 us); the mma.sync kernel's split
-  // gives equal page quotas.
-  const int seg_cost = algo == QKVP_ALGO_TCGEN05 ? kTcSegmentCost : 0;
+  // 192 us, 44 x 32K 515 -> 509 us, NVFP4 10 x 160K 568 -> 550 us). BF16 pools (the cast-then-attend
+  // baseline) take about three times longer per page, so a request start costs them little and equal
+  // quotas balance better (mixed batch 500 us against 522 us with the charge); the mma.sync kernel's
+  // split gives equal page quotas too.
+  const int seg_cost = algo == QKVP_ALGO_TCGEN05 && kv_dtype != QKVP_KV_BF16 ? kTcSegmentCost : 0;
   // count the segments, then fill the table arrays
   SplitInfo info;
   split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, SplitOut{}, info, seg_cost);
