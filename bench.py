@@ -233,20 +233,20 @@ def with_heads(w, heads: int):
     return dataclasses.replace(w, q=w.q[:, :heads, :].contiguous(), heads=heads)
 
 
-def heads_sweep(q, pk, w, kv, args, steps, g=1.0, min_splits=0, heads=(16, 32, 64)):
+def heads_sweep(q, pk, w, kv, args, steps, g=1.0, min_splits=0, heads=(16, 32, 64), algo=None):
     """Decode of one workload shape at fewer query heads, with the kernel family the planner picks for
     that head count. The KV bytes stay the same while the flops shrink, so the step moves from the
     tensor-bound to the HBM-bound side of the roofline."""
     out = {}
     for h in heads:
-        pb = Problem(q, with_heads(w, h), kv, g=g, min_splits=min_splits, algo=args.algo)
+        pb = Problem(q, with_heads(w, h), kv, g=g, min_splits=min_splits, algo=args.algo if algo is None else algo)
         r = measure(pb, steps, args.warmup, pk)
         t_hbm = pb.kv_bytes / (pk["hbm_gbs"] * 1e9) * 1e6
         t_tc = pb.flops / (pk["bf16_tflops"] * 1e12) * 1e6
         r["binding"] = "hbm" if t_hbm >= t_tc else "tensor"
         r["floor_us"] = round(max(t_hbm, t_tc), 2)
         r["frac_of_binding_floor"] = round(max(t_hbm, t_tc) / r["decode_kernel_us"], 4)
-        r["algo"] = "tcgen05" if pb.plan.algo == 2 else "mma_sync"
+        r["algo"] = {1: "mma_sync", 2: "tcgen05", 3: "mma_sync_fp8_qk"}[pb.plan.algo]
         out[f"h{h}"] = r
         del pb
     torch.cuda.empty_cache()
@@ -649,7 +649,7 @@ def profile_main(args):
     pb.check(f"profile {args.profile}")
     r = summarize(pb, ms, att, pk)
     r.update({"workload": args.profile, "heads": w.heads, "kv": args.kv,
-              "algo": "tcgen05" if pb.plan.algo == 2 else "mma_sync", "kernel_digest": kernel_source_digest(
+              "algo": {1: "mma_sync", 2: "tcgen05", 3: "mma_sync_fp8_qk"}[pb.plan.algo], "kernel_digest": kernel_source_digest(
                   "decode_tc.cu" if pb.plan.algo == 2 else "decode_mma.cu")})
     print(json.dumps(r), flush=True)
 
@@ -666,6 +666,9 @@ def extra_workloads(q, pk, dev, args, main_w=None):
         del pt
         res["heads_sweep_mla_fp8_per_token_b44_l32k"] = heads_sweep(q, pk, main_w, q.KV_FP8_PER_TOKEN, args, steps,
                                                                    heads=(16,))
+        # the FP8 Q.K^T variant (two-term E4M3 Q against the page's bytes; opt-in, slower on this GPU)
+        res["heads_sweep_mla_fp8_b44_l32k_fp8_qk"] = heads_sweep(q, pk, main_w, q.KV_FP8_E4M3, args, steps,
+                                                                heads=(16, 32), algo=q.ALGO_MMA_FP8)
         torch.cuda.empty_cache()
     # NVFP4, 10 x 163,840 (+1 appended per step), 128 heads
     w = synth.workload("mla_nvfp4_b10_h128_l160k", device=dev)

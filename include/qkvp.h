@@ -83,9 +83,21 @@ typedef enum { QKVP_SRC_FP8_E4M3 = 1, QKVP_SRC_BF16 = 2 } qkvp_src_dtype;
 typedef enum {
   QKVP_ALGO_AUTO = 0,
   QKVP_ALGO_MMA_SYNC = 1,  /* warp-level mma.sync split-KV kernel, any supported head count */
-  QKVP_ALGO_TCGEN05 = 2    /* tcgen05/TMEM CTA-pair split-KV kernel: always 128 head rows (fewer heads
+  QKVP_ALGO_TCGEN05 = 2,   /* tcgen05/TMEM CTA-pair split-KV kernel: always 128 head rows (fewer heads
                               ride as zero rows), so its cost does not shrink with the heads; AUTO picks
                               it at 64 heads and more, the mma.sync kernel below */
+  QKVP_ALGO_MMA_FP8 = 3    /* the mma.sync kernel with Q.K^T on the FP8 tensor-core path, for FP8 and
+                              per-token-scaled FP8 pools (others: QKVP_E_UNSUPPORTED): K is the page's
+                              E4M3 bytes as stored, Q is split per head row into two E4M3 terms,
+                              q ~ (hi + lo / 16) / sc with sc = 2^floor(log2(448 / max|q|)),
+                              hi = E4M3(q sc), lo = E4M3(16 (q sc - hi)), and the two products are
+                              summed in FP32; P.V stays FP16. The pages' decode dequantizes "to FP8 or
+                              BF16" ("SGLang x Qwen x NVIDIA ... NVFP4 KV Cache", section "SGLang
+                              implementation", item 3); a single E4M3 term for Q (or for P) misses
+                              the output tolerance on the outlier-channel workloads, two terms for Q
+                              meet it. 16 or 32 heads per CTA. On GB300 it takes 1.5-1.8x the
+                              time of QKVP_ALGO_MMA_SYNC (two MMAs per 32 dims, and the legacy FP8
+                              MMA path gains no rate over FP16), so AUTO never picks it. */
 } qkvp_algo;
 
 #define QKVP_LATENT_DIM 576

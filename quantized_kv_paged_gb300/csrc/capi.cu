@@ -133,7 +133,9 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   // the heads, is faster (measured on the 44 x 32K FP8 workload: 16 heads 333 us, 32 heads 435 us,
   // 64 heads 653 us, against ~560 us for the tcgen05 kernel).
   if (algo == QKVP_ALGO_AUTO) algo = num_heads >= 64 ? QKVP_ALGO_TCGEN05 : QKVP_ALGO_MMA_SYNC;
-  if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05) return QKVP_E_UNSUPPORTED;
+  if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05 && algo != QKVP_ALGO_MMA_FP8) return QKVP_E_UNSUPPORTED;
+  if (algo == QKVP_ALGO_MMA_FP8 && kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_FP8_PER_TOKEN)
+    return QKVP_E_UNSUPPORTED;
   int cpw, workers;
   if (algo == QKVP_ALGO_TCGEN05) {
     // one worker = one CTA pair; by default as many pairs as the device runs at once
@@ -149,7 +151,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
       num_sms = query_sms();
       if (num_sms <= 0) return QKVP_E_CUDA;
     }
-    const int hc = mma_heads_per_cta(num_heads);
+    const int hc = algo == QKVP_ALGO_MMA_FP8 ? mma_fp8_heads_per_cta(num_heads) : mma_heads_per_cta(num_heads);
     if (hc == 0) return QKVP_E_UNSUPPORTED;
     cpw = num_heads / hc;
     workers = std::max(1, num_sms / cpw);
@@ -237,6 +239,7 @@ DecodeArgs make_args(const qkvp_plan* plan, const void* q, const void* kv_data, 
   a.ctas_per_worker = plan->ctas_per_worker;
   a.num_segments = plan->num_segments;
   a.kv_dtype = plan->kv_dtype;
+  a.fp8_qk = plan->algo == QKVP_ALGO_MMA_FP8 ? 1 : 0;
   a.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * global_scale * 1.4426950408889634);
   a.out_scale = global_scale;
   return a;

@@ -247,8 +247,38 @@ __device__ __forceinline__ void dequant_page(const uint8_t* s_raw, uint8_t* s_kv
   }
 }
 
-template <int KV, int HC>
+// ---- FP8 Q.K^T (QKVP_ALGO_MMA_FP8): Q as two E4M3 terms, K straight from the FP8 page ----
+// D += A B, m16n8k32, E4M3 inputs, FP32 accumulators. A (16 x 32, row): a0 / a1 rows g and g + 8 of
+// k 4t .. 4t + 3, a2 / a3 the same rows at k 16 + 4t ..; B (32 x 8, col): b0 k 4t .. 4t + 3, b1 k 16 +
+// 4t .. of column g (g = lane / 4, t = lane % 4); D as for m16n8k16.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The power of two sc = 2^floor(log2(448 / max|q|)) of a head row from its largest |q| (BF16 magnitude
+// bits): the row times sc has its largest magnitude in (224, 448]. All-zero and non-finite rows use 1.
+__device__ __forceinline__ float f8_row_scale(uint32_t mbits) {
+  if (mbits == 0u || mbits >= 0x7F80u) return 1.0f;
+  const float x = __fdiv_rn(448.0f, __uint_as_float(mbits << 16));   // exact IEEE quotient
+  const int e = static_cast<int>((__float_as_uint(x) >> 23) & 0xFFu);  // floor(log2(x)) + 127 (x normal)
+  return __uint_as_float(static_cast<uint32_t>(min(max(e, 1), 254)) << 23);
+}
+
+// Two FP32 values scaled into E4M3 range -> (hi pair, lo pair): hi = E4M3(x), lo = E4M3(16 (x - hi)),
+// both rounded to nearest even (the difference and the factor 16 are exact in FP32). Low byte = x0.
+__device__ __forceinline__ void f8_two_term(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = dev::f32x2_to_e4m3x2(x0, x1);
+  const uint32_t d = dev::e4m3x2_to_f16x2(static_cast<uint16_t>(hi));
+  const float d0 = __half2float(__ushort_as_half(static_cast<unsigned short>(d & 0xFFFFu)));
+  const float d1 = __half2float(__ushort_as_half(static_cast<unsigned short>(d >> 16)));
+  lo = dev::f32x2_to_e4m3x2((x0 - d0) * 16.0f, (x1 - d1) * 16.0f);
+}
+
+template <int KV, int HC, bool F8>
 __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kv_map) {
+  static_assert(!F8 || ((KV == KV_FP8 || KV == KV_FP8PT) && HC <= 32), "FP8 Q.K^T: FP8 pools, 16 or 32 heads per CTA");
   constexpr int NG = HC / 16;       // 16-head groups in this CTA
   // With few heads the page's 64 tokens are split among warp pairs too, so that all 8 warps do
   // math: TG token groups of TPG tokens, each pair with its own softmax state, merged at the end
@@ -298,6 +328,9 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
 
   // ldmatrix lane addresses (bytes, relative to the tile bases)
   const uint32_t q_lane = ((grp * 16 + (lane & 15)) * kRow + (lane >> 4) * 8) * 2;
+  // FP8 Q planes: row r keeps its hi bytes at [0, 576) and its lo bytes at [576, 1152) of the row
+  const uint32_t q8_lane = (grp * 16 + (lane & 15)) * kRowBytes + (lane >> 4) * 16;
+  float qf8[2] = {0.0f, 0.0f};      // FP8 Q.K^T: logit factor (sm_scale g log2 e / sc) of rows g8, g8 + 8
   const uint32_t k_lane = (((lane & 7) + ((lane >> 4) << 3)) * kRow + ((lane >> 3) & 1) * 8) * 2;
   const uint32_t v_lane = (((lane & 7) + ((lane >> 3) & 1) * 8) * kRow + half * 256 + (lane >> 4) * 8) * 2;
   float* const x_mine0 = s_x + (pi * 2 + half) * XF;
@@ -310,17 +343,22 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
     __syncthreads();  // the previous segment is done with s_q / s_kv / s_raw
     if (seg.req != cur_req) {
       const uint8_t* gq = reinterpret_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(seg.req) * a.heads + h0) * kLatent * 2;
+      // (the FP8 Q.K^T stages the BF16 rows densely in the first raw buffer, free until this
+      // segment's pages are fetched, and converts them into the Q area)
       for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
         const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
-        dev::cp_async16(a_q + row * kRowBytes + ch * 16, gq + static_cast<int64_t>(row) * kLatent * 2 + ch * 16);
+        const uint32_t dst = F8 ? a_raw + row * (kLatent * 2) + ch * 16 : a_q + row * kRowBytes + ch * 16;
+        dev::cp_async16(dst, gq + static_cast<int64_t>(row) * kLatent * 2 + ch * 16);
       }
       dev::cp_async_commit();
       if (tid == 0) *s_qmax = 0u;
+      if (F8)
+        for (int r = tid; r < HC; r += NT) reinterpret_cast<uint32_t*>(s_x)[r] = 0u;
       dev::cp_async_wait_all();
       __syncthreads();
       // largest |q| of this CTA's heads, as BF16 magnitude bits (integer order = magnitude order)
       uint32_t mx = 0;
-      for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
+      for (int c = F8 ? NT * HC * kLatent : tid; c < HC * (kLatent * 2 / 16); c += NT) {
         const int row = c / (kLatent * 2 / 16), ch = c % (kLatent * 2 / 16);
         const uint4 v = *reinterpret_cast<const uint4*>(s_q + row * kRowBytes + ch * 16);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -336,7 +374,48 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       if (qm != 0u && qm < 0x7F80u) sh = max(-100, min(113, static_cast<int>(qm >> 7) - 127 - 14));
       const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
       q_scale_log2 = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
-      if constexpr (RAW && KV == KV_NVFP4) {
+      if constexpr (F8) {
+        // Q as two E4M3 terms per head row (sc = f8_row_scale of the row's largest |q|):
+        // hi = E4M3(q sc), lo = E4M3(16 (q sc - hi)), q ~ (hi + lo / 16) / sc, from the BF16 rows
+        // staged in the first raw buffer into the Q area (hi at bytes [0, 576) of a row, lo at
+        // [576, 1152)).
+        static_assert(!F8 || HC * kLatent * 2 <= raw_bytes<KV>(), "Q staging fits one raw buffer");
+        const uint8_t* qst = s_raw;
+        uint32_t* rmax = reinterpret_cast<uint32_t*>(s_x);
+        for (int c = tid; c < HC * (kLatent * 2 / 16); c += NT) {
+          const int row = c / (kLatent * 2 / 16);
+          const uint4 v = reinterpret_cast<const uint4*>(qst)[c];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t m = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m = max(m, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+          atomicMax(rmax + row, m);
+        }
+        __syncthreads();
+        for (int c = tid; c < HC * (kLatent / 16); c += NT) {
+          const int row = c / (kLatent / 16), ch = c % (kLatent / 16);
+          const float sc = f8_row_scale(rmax[row]);
+          const uint4 v0 = reinterpret_cast<const uint4*>(qst)[2 * c];
+          const uint4 v1 = reinterpret_cast<const uint4*>(qst)[2 * c + 1];
+          const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          uint32_t hv[4], lv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {       // dims 4k .. 4k + 3 of the chunk
+            uint32_t h01, l01, h23, l23;
+            f8_two_term(__uint_as_float(w[2 * k] << 16) * sc, __uint_as_float(w[2 * k] & 0xFFFF0000u) * sc, h01, l01);
+            f8_two_term(__uint_as_float(w[2 * k + 1] << 16) * sc, __uint_as_float(w[2 * k + 1] & 0xFFFF0000u) * sc, h23, l23);
+            hv[k] = (h01 & 0xFFFFu) | (h23 << 16);
+            lv[k] = (l01 & 0xFFFFu) | (l23 << 16);
+          }
+          *reinterpret_cast<uint4*>(s_q + row * kRowBytes + ch * 16) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          *reinterpret_cast<uint4*>(s_q + row * kRowBytes + kLatent + ch * 16) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t m = rmax[grp * 16 + g8 + 8 * r];
+          qf8[r] = m >= 0x7F80u ? __uint_as_float(0x7FC00000u) : __fdiv_rn(a.scale_log2, f8_row_scale(m));
+        }
+      } else if constexpr (RAW && KV == KV_NVFP4) {
         // NVFP4 raw-operand path: within every 32 dims (16 dim pairs), pair position i holds pair
         // 4(i % 4) + i / 4, the order a lane's K fragment bytes come in (a 4 x 4 transpose)
         for (int c = tid; c < HC * (kLatent / 32); c += NT) {
@@ -375,7 +454,9 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         }
       }
       cur_req = seg.req;
-      // the conversion is made visible to every warp by the barrier before the first page
+      // every warp reads Q (ldmatrix) only after every thread's conversion (and, for the FP8 Q.K^T,
+      // its read of the row maxima in the exchange buffer) is done
+      __syncthreads();
     }
     float o[32][4];
 #pragma unroll
@@ -492,7 +573,47 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
       float s[2 * NPI][4];
 #pragma unroll
       for (int n = 0; n < 2 * NPI; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
-      if constexpr (RAW && KV == KV_NVFP4) {
+      if constexpr (F8) {
+        // FP8 Q.K^T: per 32-dim k-step an m16n8k32 E4M3 MMA with the hi plane of Q into s and one with
+        // the lo plane into s2, both with the page's own bytes as B. The byte ldmatrix of the raw
+        // path gives lane l, per 16-dim chunk, dims 4t4 .. 4t4 + 3 of the row of logit column g8:
+        // chunks 2u and 2u + 1 of a block of four are the b0 / b1 of k-step u. Q needs no permutation.
+        const int kr = lane & 7;
+        float s2[2 * NPI][4];
+#pragma unroll
+        for (int n = 0; n < 2 * NPI; ++n) s2[n][0] = s2[n][1] = s2[n][2] = s2[n][3] = 0.0f;
+#pragma unroll
+        for (int kb = 0; kb < 5; ++kb) {       // 16-dim chunks 4kb .. 4kb + 3 of the half (two in the last)
+          uint32_t ah[2][4], al[2][4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (2 * kb + u < 9) {
+              const uint32_t qa = a_q + q8_lane + half * 288 + 32 * (2 * kb + u);
+              dev::ldsm_x4(qa, ah[u][0], ah[u][1], ah[u][2], ah[u][3]);
+              dev::ldsm_x4(qa + kLatent, al[u][0], al[u][1], al[u][2], al[u][3]);
+            }
+#pragma unroll
+          for (int p = 0; p < NPI; ++p)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const uint32_t addr = trb(p) + raw_chunk_off(tt0(p) + rho(4 * (kr >> 1) + (kr & 1) + 2 * jj),
+                                                           half * 18 + 4 * kb + (lane >> 3));
+              uint32_t r[4];
+              if (kb < 4) dev::ldsm_x4(addr, r[0], r[1], r[2], r[3]);
+              else dev::ldsm_x2(addr, r[0], r[1]);
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                if (2 * kb + u >= 9) continue;
+                mma_e4m3(s[2 * p + jj], ah[u], r[2 * u], r[2 * u + 1]);
+                mma_e4m3(s2[2 * p + jj], al[u], r[2 * u], r[2 * u + 1]);
+              }
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < 2 * NPI; ++n)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s[n][i] = fmaf(s2[n][i], 0.0625f, s[n][i]);
+      } else if constexpr (RAW && KV == KV_NVFP4) {
         // NVFP4: a 16-byte chunk c of a row is 32 dims, two 16-element blocks. As for FP8, lane l
         // addresses row rho(4((l & 7) >> 1) + (l & 1) + 2jj) of tile p, chunk (l >> 3) of a pair; it
         // receives bytes 4t4 .. 4t4+3 of the row of logit column g8: dims 32c + 8t4 .. +7, all in
@@ -637,7 +758,7 @@ __global__ void __launch_bounds__(kNT, 1) decode_mma_kernel(const DecodeArgs a, 
         for (int i = 0; i < 4; ++i) {
           const int tok = tok_of(n, i & 1);
           const float x = KV == KV_FP8PT ? s[n][i] * sig[n][i & 1] : s[n][i];
-          const float v = tok < (RAW ? tlive(n >> 1) : live) ? x * q_scale_log2 : -INFINITY;
+          const float v = tok < (RAW ? tlive(n >> 1) : live) ? x * (F8 ? qf8[i >> 1] : q_scale_log2) : -INFINITY;
           s[n][i] = v;
           mx[i >> 1] = fmaxf(mx[i >> 1], v);
         }
@@ -880,12 +1001,12 @@ cudaError_t encode_kv_map(const DecodeArgs& a, int64_t row_bytes, int64_t page_b
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int KV, int HC>
+template <int KV, int HC, bool F8 = false>
 cudaError_t launch_kv_hc(const DecodeArgs& a, cudaStream_t s) {
   constexpr int smem = smem_bytes<KV, HC>();
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<KV, HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<KV, HC, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -897,12 +1018,22 @@ cudaError_t launch_kv_hc(const DecodeArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = static_cast<unsigned>(a.num_workers * a.ctas_per_worker);
-  decode_mma_kernel<KV, HC><<<grid, kNT, smem, s>>>(a, map);
+  decode_mma_kernel<KV, HC, F8><<<grid, kNT, smem, s>>>(a, map);
   return cudaGetLastError();
 }
 
 template <int KV>
 cudaError_t launch_kv(const DecodeArgs& a, cudaStream_t s) {
+  if constexpr (KV == KV_FP8 || KV == KV_FP8PT) {
+    if (a.fp8_qk) {
+      switch (mma_fp8_heads_per_cta(a.heads)) {
+        case 16: return launch_kv_hc<KV, 16, true>(a, s);
+        case 32: return launch_kv_hc<KV, 32, true>(a, s);
+        default: return cudaErrorInvalidValue;
+      }
+    }
+  }
+  if (a.fp8_qk) return cudaErrorInvalidValue;
   switch (mma_heads_per_cta(a.heads)) {
     case 16: return launch_kv_hc<KV, 16>(a, s);
     case 32: return launch_kv_hc<KV, 32>(a, s);
@@ -913,6 +1044,11 @@ cudaError_t launch_kv(const DecodeArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+int mma_fp8_heads_per_cta(int heads) {
+  if (heads < 16 || heads > 128 || heads % 16) return 0;
+  return heads % 32 == 0 ? 32 : 16;
+}
 
 int mma_heads_per_cta(int heads) {
   if (heads < 16 || heads > 128 || heads % 16) return 0;

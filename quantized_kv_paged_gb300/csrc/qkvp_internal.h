@@ -54,6 +54,7 @@ struct DecodeArgs {
   float* lse;                 // [B][H] natural log, may be null
   int* status;                // device status word (timeouts), inside the workspace
   int batch, heads, num_workers, ctas_per_worker, num_segments, kv_dtype;
+  int fp8_qk;                 // mma.sync kernel: FP8 Q.K^T (two-term E4M3 Q) instead of FP16
   float scale_log2;           // sm_scale * g * log2(e)
   float out_scale;            // g
 };
@@ -142,8 +143,10 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int num_wide, cudaStream_t s);
 
-// Heads per CTA of the mma.sync kernel for a head count (0 if unsupported).
+// Heads per CTA of the mma.sync kernel for a head count (0 if unsupported), and of its FP8 Q.K^T
+// variant (16 or 32).
 int mma_heads_per_cta(int heads);
+int mma_fp8_heads_per_cta(int heads);
 // CTA pairs of the tcgen05 kernel that the current device runs at once (-1 on error).
 int tc_max_active_clusters();
 

@@ -227,3 +227,15 @@ def test_tcgen05_split_charges_request_starts(lib):
     a, b = plan(sp, sl, algo=q.ALGO_TCGEN05), plan(sp, sl, algo=q.ALGO_MMA_SYNC)
     assert b.num_segments == 145 and b.max_worker_pages == 93
     assert a.num_segments == 70 and a.max_worker_pages == 100 and a.min_worker_pages == 0
+
+
+def test_fp8_qk_algo_plans_fp8_pools_only(lib):
+    ptr, lens = np.array([0, 2], np.int32), np.array([100], np.int32)
+    for kv in (q.KV_FP8_E4M3, q.KV_FP8_PER_TOKEN):
+        for heads, per_cta in ((16, 16), (32, 32), (48, 16), (64, 32), (128, 32)):
+            p = plan(ptr, lens, heads=heads, kv=kv, algo=q.ALGO_MMA_FP8)
+            assert p.status == q.QKVP_OK and p.algo == q.ALGO_MMA_FP8
+            assert p.ctas_per_worker == heads // per_cta
+    for kv in (q.KV_NVFP4, q.KV_BF16):
+        assert plan(ptr, lens, kv=kv, algo=q.ALGO_MMA_FP8).status == q.QKVP_E_UNSUPPORTED
+    assert plan(ptr, lens, heads=128).algo == q.ALGO_TCGEN05            # never picked by AUTO

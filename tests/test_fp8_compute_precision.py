@@ -13,6 +13,8 @@ encoder. Outcomes, against the stated bound (max-abs 2e-2 over half a BF16 ulp):
   - Q as a two-term E4M3 sum (q = hi + lo / 16) with FP16 P: within the bound. That split doubles the
     Q.K^T MMAs, which is the FP16 MMA count again: FP8 operands cannot raise the tensor ceiling of
     this decode within the tolerance.
+The two-term form is the library's FP8 Q.K^T variant (QKVP_ALGO_MMA_FP8); its GPU parity tests are in
+test_gpu_decode.py.
 """
 import numpy as np
 import pytest

@@ -191,3 +191,44 @@ def test_full_nvfp4_b1_l1m(qkvp, g_mode):
 @pytest.mark.parametrize("kv", [FP8, BF16])
 def test_full_mixed_pool(qkvp, kv):
     _full_check("mla_fp8_mixed_b64_h128_pool495552", kv, n_pairs=16, algo=q.ALGO_MMA_SYNC)
+
+
+# ---- FP8 Q.K^T (QKVP_ALGO_MMA_FP8): two-term E4M3 Q against the page's E4M3 bytes -------------------
+
+F8QK = q.ALGO_MMA_FP8
+
+
+@pytest.mark.parametrize("heads", [16, 32, 48, 128])
+@pytest.mark.parametrize("kv", [FP8, FP8PT])
+def test_fp8_qk_ragged_batch(qkvp, heads, kv):
+    """The FP8 Q.K^T variant meets the same tolerance against the FP64 oracle as the FP16 kernels, on
+    ragged batches with x20 outlier channels, empty requests and split requests."""
+    lens = [1, 63, 64, 65, 200, 0, 1000, 4097, 129]
+    w = synth.build_workload("ragged_f8", lens, heads=heads, pool_pages=180, seed=70 + heads + kv,
+                             outliers=4, device="cuda", extra_pages=[1] * len(lens))
+    for sms in (4, 37, 152):
+        out, lse, plan = gpu_decode(w, kv, gpu_pools(w, kv), algo=F8QK, num_sms=sms)
+        assert plan.algo == F8QK and plan.ctas_per_worker == heads // (32 if heads % 32 == 0 else 16)
+        o_ref, lse_ref = oracle_decode(w, kv, oracle_pools(w, kv))
+        compare(out.float().cpu().numpy().reshape(-1, 512), lse.cpu().numpy().reshape(-1), o_ref, lse_ref)
+
+
+def test_fp8_qk_q_rows_of_any_magnitude(qkvp):
+    """Each head row gets its own power-of-two scale into the E4M3 range: rows at 2^15, one element of
+    40,000, rows below 1 and at 2^-40 all meet the tolerance."""
+    import dataclasses
+    w = synth.build_workload("qrange_f8", [300, 64, 1000], heads=32, pool_pages=40, seed=12, outliers=4,
+                             device="cuda", extra_pages=[1] * 3)
+    x = w.q.float()
+    x[0, 3] *= 2.0 ** 14
+    x[0, 9, 17] = 40000.0
+    x[1, 7] *= 2.0 ** -12
+    x[2, 10] *= 2.0 ** -40
+    w = dataclasses.replace(w, q=x.to(torch.bfloat16))
+    out, lse, _ = gpu_decode(w, FP8, gpu_pools(w, FP8), algo=F8QK, num_sms=37)
+    o_ref, lse_ref = oracle_decode(w, FP8, oracle_pools(w, FP8))
+    compare(out.float().cpu().numpy().reshape(-1, 512), lse.cpu().numpy().reshape(-1), o_ref, lse_ref)
+
+
+def test_full_fp8_b44_l32k_fp8_qk(qkvp):
+    _full_check("mla_fp8_b44_h128_l32k", FP8, algo=F8QK)
