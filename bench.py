@@ -57,6 +57,11 @@ def peaks():
     return p
 
 
+# kernel families of the plan's algo field, and the translation unit of each
+ALGO_NAMES = {1: "mma_sync", 2: "tcgen05", 3: "mma_sync_fp8_qk", 4: "tcgen05_tokens"}
+ALGO_SOURCES = {1: "decode_mma.cu", 2: "decode_tc.cu", 3: "decode_mma.cu", 4: "decode_tm.cu"}
+
+
 def kernel_source_digest(tu: str = "decode_tc.cu"):
     """Digest of the sources the timed decode kernel is compiled from: its translation unit and the
     library headers (a change elsewhere in the library does not change this kernel)."""
@@ -246,7 +251,7 @@ def heads_sweep(q, pk, w, kv, args, steps, g=1.0, min_splits=0, heads=(16, 32, 6
         r["binding"] = "hbm" if t_hbm >= t_tc else "tensor"
         r["floor_us"] = round(max(t_hbm, t_tc), 2)
         r["frac_of_binding_floor"] = round(max(t_hbm, t_tc) / r["decode_kernel_us"], 4)
-        r["algo"] = {1: "mma_sync", 2: "tcgen05", 3: "mma_sync_fp8_qk"}[pb.plan.algo]
+        r["algo"] = ALGO_NAMES[pb.plan.algo]
         out[f"h{h}"] = r
         del pb
     torch.cuda.empty_cache()
@@ -649,8 +654,7 @@ def profile_main(args):
     pb.check(f"profile {args.profile}")
     r = summarize(pb, ms, att, pk)
     r.update({"workload": args.profile, "heads": w.heads, "kv": args.kv,
-              "algo": {1: "mma_sync", 2: "tcgen05", 3: "mma_sync_fp8_qk"}[pb.plan.algo], "kernel_digest": kernel_source_digest(
-                  "decode_tc.cu" if pb.plan.algo == 2 else "decode_mma.cu")})
+              "algo": ALGO_NAMES[pb.plan.algo], "kernel_digest": kernel_source_digest(ALGO_SOURCES[pb.plan.algo])})
     print(json.dumps(r), flush=True)
 
 

@@ -86,7 +86,7 @@ typedef enum {
   QKVP_ALGO_TCGEN05 = 2,   /* tcgen05/TMEM CTA-pair split-KV kernel: always 128 head rows (fewer heads
                               ride as zero rows), so its cost does not shrink with the heads; AUTO picks
                               it at 64 heads and more, the mma.sync kernel below */
-  QKVP_ALGO_MMA_FP8 = 3    /* the mma.sync kernel with Q.K^T on the FP8 tensor-core path, for FP8 and
+  QKVP_ALGO_MMA_FP8 = 3,   /* the mma.sync kernel with Q.K^T on the FP8 tensor-core path, for FP8 and
                               per-token-scaled FP8 pools (others: QKVP_E_UNSUPPORTED): K is the page's
                               E4M3 bytes as stored, Q is split per head row into two E4M3 terms,
                               q ~ (hi + lo / 16) / sc with sc = 2^floor(log2(448 / max|q|)),
@@ -98,6 +98,15 @@ typedef enum {
                               meet it. 16 or 32 heads per CTA. On GB300 it takes 1.5-1.8x the
                               time of QKVP_ALGO_MMA_SYNC (two MMAs per 32 dims, and the legacy FP8
                               MMA path gains no rate over FP16), so AUTO never picks it. */
+  QKVP_ALGO_TCGEN05_TOKENS = 4 /* tcgen05/TMEM kernel with the page's tokens as the rows of both
+                              products (M = 64 tokens for Q.K^T, M = 128 output dims for P.V) and the
+                              heads as the columns (N = 16, 32 or 64; 48 heads ride in 64): 16 to 64
+                              heads, FP8, NVFP4 and per-token-scaled FP8 pools (others:
+                              QKVP_E_UNSUPPORTED); one CTA per SM. Same arithmetic and tolerance as
+                              the other families. Measured on GB300 it is faster than AUTO's choice
+                              only for NVFP4 pools at 32 heads (10 x 160K: 479 us against 542 us);
+                              elsewhere slower (FP8 44 x 32K at 16 / 32 / 64 heads: 292 / 440 /
+                              918 us against 201 / 312 / 494 us), so AUTO never picks it. */
 } qkvp_algo;
 
 #define QKVP_LATENT_DIM 576

@@ -20,7 +20,7 @@ QKVP_OK, QKVP_E_INVALID, QKVP_E_UNSUPPORTED, QKVP_E_WORKSPACE, QKVP_E_CUDA = 0, 
 KV_FP8_E4M3, KV_NVFP4, KV_BF16, KV_FP8_PER_TOKEN = 1, 2, 3, 4
 PAGE_BYTES_FP8_PER_TOKEN = 64 * (576 + 4)   # 64 rows of E4M3 codes, then 64 FP32 token scales
 SRC_FP8_E4M3, SRC_BF16 = 1, 2
-ALGO_AUTO, ALGO_MMA_SYNC, ALGO_TCGEN05, ALGO_MMA_FP8 = 0, 1, 2, 3
+ALGO_AUTO, ALGO_MMA_SYNC, ALGO_TCGEN05, ALGO_MMA_FP8, ALGO_TCGEN05_TOKENS = 0, 1, 2, 3, 4
 LATENT_DIM, V_DIM, PAGE_SIZE = 576, 512, 64
 
 EXPORTS = ["kv_append_quant", "mla_decode_plan", "mla_decode_run", "mla_decode_attend",

@@ -133,11 +133,23 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   // the heads, is faster (measured on the 44 x 32K FP8 workload: 16 heads 333 us, 32 heads 435 us,
   // 64 heads 653 us, against ~560 us for the tcgen05 kernel).
   if (algo == QKVP_ALGO_AUTO) algo = num_heads >= 64 ? QKVP_ALGO_TCGEN05 : QKVP_ALGO_MMA_SYNC;
-  if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05 && algo != QKVP_ALGO_MMA_FP8) return QKVP_E_UNSUPPORTED;
+  if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05 && algo != QKVP_ALGO_MMA_FP8 &&
+      algo != QKVP_ALGO_TCGEN05_TOKENS)
+    return QKVP_E_UNSUPPORTED;
   if (algo == QKVP_ALGO_MMA_FP8 && kv_dtype != QKVP_KV_FP8_E4M3 && kv_dtype != QKVP_KV_FP8_PER_TOKEN)
     return QKVP_E_UNSUPPORTED;
+  if (algo == QKVP_ALGO_TCGEN05_TOKENS && (kv_dtype == QKVP_KV_BF16 || tm_heads_padded(num_heads) == 0))
+    return QKVP_E_UNSUPPORTED;
   int cpw, workers;
-  if (algo == QKVP_ALGO_TCGEN05) {
+  if (algo == QKVP_ALGO_TCGEN05_TOKENS) {
+    // one worker = one CTA, one CTA per SM
+    cpw = 1;
+    if (num_sms <= 0) {
+      num_sms = query_sms();
+      if (num_sms <= 0) return QKVP_E_CUDA;
+    }
+    workers = num_sms;
+  } else if (algo == QKVP_ALGO_TCGEN05) {
     // one worker = one CTA pair; by default as many pairs as the device runs at once
     cpw = 2;
     if (num_sms <= 0) {
@@ -260,7 +272,9 @@ int mla_decode_attend(const qkvp_plan* plan, const void* q, const void* kv_data,
   const DecodeArgs a = make_args(plan, q, kv_data, kv_scale, num_pages, kv_indices, sm_scale,
                                  global_scale, out, lse, workspace);
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = plan->algo == QKVP_ALGO_TCGEN05 ? launch_decode_tc(a, st_) : launch_decode_mma(a, st_);
+  cudaError_t e = plan->algo == QKVP_ALGO_TCGEN05          ? launch_decode_tc(a, st_)
+                  : plan->algo == QKVP_ALGO_TCGEN05_TOKENS ? launch_decode_tm(a, st_)
+                                                           : launch_decode_mma(a, st_);
   return e == cudaSuccess ? QKVP_OK : QKVP_E_CUDA;
 }
 

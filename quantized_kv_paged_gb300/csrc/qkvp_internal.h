@@ -141,12 +141,15 @@ cudaError_t launch_encode(const float* x, int64_t n, int fmt, uint8_t* codes, cu
 cudaError_t launch_cast(const uint8_t* in, int64_t n, uint16_t* out, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_tm(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int num_wide, cudaStream_t s);
 
 // Heads per CTA of the mma.sync kernel for a head count (0 if unsupported), and of its FP8 Q.K^T
 // variant (16 or 32).
 int mma_heads_per_cta(int heads);
 int mma_fp8_heads_per_cta(int heads);
+// Head columns of the token-major tcgen05 kernel for a head count (16, 32 or 64; 0 if unsupported).
+int tm_heads_padded(int heads);
 // CTA pairs of the tcgen05 kernel that the current device runs at once (-1 on error).
 int tc_max_active_clusters();
 

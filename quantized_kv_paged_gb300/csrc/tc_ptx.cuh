@@ -49,6 +49,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: a thread whose phase is not complete may sleep up to `ns`
+// nanoseconds (it wakes when the phase completes), so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
@@ -205,6 +216,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// 32 lanes x 16 columns: thread i reads lane (taddr.lane + i), columns taddr.col .. + 15.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 // kMemoryOrder = false: no compiler memory barrier, so ordinary loads may be scheduled across the
 // store (it reads registers only); ordering with other tcgen05 instructions is kept.
 template <bool kMemoryOrder = true>
@@ -330,6 +360,11 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t chunk
 // 64-byte swizzle: rows of 64 bytes, chunk index XOR ((row / 2) mod 4); atoms of 512 bytes.
 __host__ __device__ constexpr uint32_t sw64_offset(uint32_t row, uint32_t chunk) {
   return (row >> 3) * 512u + (row & 7u) * 64u + (((chunk & 3u) ^ ((row >> 1) & 3u)) << 4);
+}
+
+// 32-byte swizzle: rows of 32 bytes, chunk index XOR ((row / 4) mod 2); atoms of 256 bytes.
+__host__ __device__ constexpr uint32_t sw32_offset(uint32_t row, uint32_t chunk) {
+  return (row >> 3) * 256u + (row & 7u) * 32u + (((chunk & 1u) ^ ((row >> 2) & 1u)) << 4);
 }
 
 }  // namespace tc

@@ -239,3 +239,19 @@ def test_fp8_qk_algo_plans_fp8_pools_only(lib):
     for kv in (q.KV_NVFP4, q.KV_BF16):
         assert plan(ptr, lens, kv=kv, algo=q.ALGO_MMA_FP8).status == q.QKVP_E_UNSUPPORTED
     assert plan(ptr, lens, heads=128).algo == q.ALGO_TCGEN05            # never picked by AUTO
+
+
+def test_token_major_algo_plans_16_to_64_heads(lib):
+    """QKVP_ALGO_TCGEN05_TOKENS: one CTA per SM (workers = SMs, one CTA each), 16-64 heads, quantized
+    pools only; AUTO never picks it."""
+    ptr, lens = np.array([0, 2], np.int32), np.array([100], np.int32)
+    for kv in (q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_FP8_PER_TOKEN):
+        for heads in (16, 32, 48, 64):
+            p = plan(ptr, lens, heads=heads, kv=kv, algo=q.ALGO_TCGEN05_TOKENS, sms=37)
+            assert p.status == q.QKVP_OK and p.algo == q.ALGO_TCGEN05_TOKENS
+            assert p.ctas_per_worker == 1 and p.num_workers == 37
+        for heads in (80, 128):
+            assert plan(ptr, lens, heads=heads, kv=kv, algo=q.ALGO_TCGEN05_TOKENS).status == q.QKVP_E_UNSUPPORTED
+    assert plan(ptr, lens, heads=32, kv=q.KV_BF16, algo=q.ALGO_TCGEN05_TOKENS).status == q.QKVP_E_UNSUPPORTED
+    for heads in (16, 32, 64):
+        assert plan(ptr, lens, heads=heads).algo != q.ALGO_TCGEN05_TOKENS

@@ -11,7 +11,7 @@ from tests.helpers import gpu_pools
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("algo", [q.ALGO_MMA_SYNC, q.ALGO_TCGEN05])
+@pytest.mark.parametrize("algo", [q.ALGO_MMA_SYNC, q.ALGO_TCGEN05, q.ALGO_TCGEN05_TOKENS])
 @pytest.mark.parametrize("kv", [q.KV_FP8_E4M3, q.KV_NVFP4])
 def test_captured_decode_replays_bit_identical(qkvp, algo, kv):
     w = synth.build_workload("graph", [700, 64, 1300, 5], heads=64, pool_pages=40, seed=31, outliers=2,
