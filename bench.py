@@ -673,6 +673,9 @@ def extra_workloads(q, pk, dev, args, main_w=None):
         # the FP8 Q.K^T variant (two-term E4M3 Q against the page's bytes; opt-in, slower on this GPU)
         res["heads_sweep_mla_fp8_b44_l32k_fp8_qk"] = heads_sweep(q, pk, main_w, q.KV_FP8_E4M3, args, steps,
                                                                 heads=(16, 32), algo=q.ALGO_MMA_FP8)
+        # the token-major tcgen05 kernel (opt-in; faster than the planner's choice only for NVFP4 at 32 heads)
+        res["heads_sweep_mla_fp8_b44_l32k_tokens"] = heads_sweep(q, pk, main_w, q.KV_FP8_E4M3, args, steps,
+                                                                 algo=q.ALGO_TCGEN05_TOKENS)
         torch.cuda.empty_cache()
     # NVFP4, 10 x 163,840 (+1 appended per step), 128 heads
     w = synth.workload("mla_nvfp4_b10_h128_l160k", device=dev)
@@ -680,6 +683,8 @@ def extra_workloads(q, pk, dev, args, main_w=None):
     res["mla_nvfp4_b10_h128_l160k"] = measure(pb, steps, args.warmup, pk)
     del pb
     res["heads_sweep_mla_nvfp4_b10_l160k"] = heads_sweep(q, pk, w, q.KV_NVFP4, args, steps)
+    res["heads_sweep_mla_nvfp4_b10_l160k_tokens"] = heads_sweep(q, pk, w, q.KV_NVFP4, args, steps,
+                                                                algo=q.ALGO_TCGEN05_TOKENS)
     nv = Problem(q, w, q.KV_NVFP4, g=1.0)
     res["extend_gather_nvfp4_b10_l160k"] = extend_gather(q, pk, w, q.KV_NVFP4, nv.data, nv.scale, 1.0, steps, args.warmup)
     res["extend_gather_fp8_b10_l160k"] = extend_gather(q, pk, w, q.KV_FP8_E4M3, w.pool_fp8, None, 1.0, steps, args.warmup)
