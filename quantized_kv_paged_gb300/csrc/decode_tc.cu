@@ -45,10 +45,19 @@
 
 #include "qkvp_device.cuh"
 #include "qkvp_internal.h"
+#include "decode_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace qkvp {
 namespace {
+
+using kern::Cursor;
+using kern::Sync;
+using kern::ldg_nc;
+using kern::ldg_nc32;
+using kern::page_ok;
+using kern::sts128;
+using kern::sts128_relaxed;
 
 constexpr int kThreads = 384;
 constexpr int kDQ = 160;                     // dequant threads (warps 4-8)
@@ -103,46 +112,6 @@ static_assert(TM_Q + kQTmemDims / 2 == TM_S && TM_S + 2 * kHalf == 512, "TMEM co
 
 constexpr uint32_t kIdescQK = tc::idesc_f16(128, kHalf, 0, 0);
 constexpr uint32_t kIdescPV = tc::idesc_f16(128, 256, 0, 1);
-
-// Walks a worker's (segment, page) sequence.
-struct Cursor {
-  int si, se, j;
-  Segment seg;
-  __device__ void begin(const DecodeArgs& a, int s0, int s1) {
-    si = s0; se = s1; j = 0;
-    if (si < se) seg = a.segs[si];
-  }
-  __device__ bool done() const { return si >= se; }
-  __device__ void next(const DecodeArgs& a) {
-    if (++j >= seg.num_pages) { j = 0; if (++si < se) seg = a.segs[si]; }
-  }
-  __device__ int valid() const { return min(kPage, seg.num_tokens - j * kPage); }
-  __device__ int64_t page(const DecodeArgs& a) const { return a.kv_indices[seg.page_begin + j]; }
-};
-
-__device__ __forceinline__ uint4 ldg_nc(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-// 32 bytes from global memory through the non-coherent path (the address must be 32-byte aligned).
-__device__ __forceinline__ void ldg_nc32(const void* p, uint32_t (&v)[8]) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-               : "l"(p));
-}
-
-// The same store without a compiler memory barrier: later global loads may be issued before it. Only
-// for shared memory that no ordinary load reads (operands the tensor cores read after a proxy fence).
-__device__ __forceinline__ void sts128_relaxed(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
 
 // ---- dequantization of a page into the two operand rings -------------------------------------
 // K slot: own tokens (rows 0..31 = tokens 32c..32c+31) x the 4 nope atoms of the other CTA's dims,
@@ -347,49 +316,6 @@ template <> struct Dequant<KV_BF16> {      // the cast-then-attend baseline: BF1
   }
 };
 
-__device__ __forceinline__ bool page_ok(const DecodeArgs& a, int64_t page) { return page >= 0 && page < a.num_pages; }
-
-struct Sync {
-  uint32_t bars;
-  volatile int* abort;
-  int* status;
-  __device__ uint32_t bar(uint32_t i) const { return bars + 8 * i; }
-  __device__ bool wait(uint32_t i, uint32_t parity, bool cluster = false, int code = 1) const {
-    const uint32_t b = bar(i);
-    if (cluster ? tc::mbar_try_wait_cluster(b, parity) : tc::mbar_try_wait(b, parity)) return true;
-    const long long t0 = clock64();
-    for (int n = 0;; ++n) {
-      if (cluster ? tc::mbar_try_wait_cluster(b, parity) : tc::mbar_try_wait(b, parity)) return true;
-      if ((n & 255) == 0) {
-        if (*abort) return false;
-        if (clock64() - t0 > (1ll << 31)) {
-          *abort = 1;
-          atomicOr(status, code);
-          return false;
-        }
-      }
-    }
-  }
-};
-
-// Bounded wait until the counter at `addr` reaches `target` (acquire: what was written before the
-// counter was raised is visible afterwards).
-__device__ bool wait_counter(const Sync& sy, uint32_t addr, uint32_t target) {
-  if (tc::ld_acquire_u32(addr) >= target) return true;
-  const long long t0 = clock64();
-  for (int n = 0;; ++n) {
-    if (tc::ld_acquire_u32(addr) >= target) return true;
-    if ((n & 255) == 0) {
-      if (*sy.abort) return false;
-      if (clock64() - t0 > (1ll << 31)) {
-        *sy.abort = 1;
-        atomicOr(sy.status, 8);
-        return false;
-      }
-    }
-  }
-}
-
 // ---- roles -------------------------------------------------------------------------------------------
 // L2 prefetch of the bytes of a page that this CTA's raw loads start from: its own 32 token rows (and
 // their scales). The peer prefetches the other 32 rows, whose 256 V dims this CTA also reads.
@@ -519,7 +445,7 @@ __device__ void role_qk(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_
     if (gq >= 2 && !sy.wait(B_S_FREE + s, ((gq >> 1) - 1) & 1, false, 4)) break;
     // the Q rows of this page's request: the qcount-th request Q published by the softmax threads
     if (q_waited != qcount) {
-      if (!wait_counter(sy, qver, static_cast<uint32_t>(qcount))) break;
+      if (!kern::wait_counter(sy, qver, static_cast<uint32_t>(qcount), 8)) break;
       q_waited = qcount;
     }
     tc::tc_fence_after();

@@ -40,16 +40,22 @@
 
 #include "qkvp_device.cuh"
 #include "qkvp_internal.h"
+#include "decode_common.cuh"
 #include "tc_ptx.cuh"
 
 namespace qkvp {
 namespace {
 
+using kern::Cursor;
+using kern::Sync;
+using kern::ldg_nc32;
+using kern::page_ok;
+using kern::sts128;
+
 constexpr int kCols = kLatent / 64;             // 64-dim atom columns of a tile
 constexpr uint32_t kColBytes = kPage * 128;     // 64 token rows x 64 FP16 dims
 constexpr uint32_t kTileBytes = kCols * kColBytes;
 constexpr int kStatusBase = 16;                 // status bits of this kernel's timeouts: 16 << role
-constexpr uint32_t kSleepNs = 20000;            // longest sleep of a waiting thread per try (it wakes on completion)
 
 enum : uint32_t {
   B_T_FULL = 0, B_T_EMPTY = 2, B_S_FULL = 4, B_S_FREE = 6, B_P_FULL = 8, B_P_FREE = 10, B_O_FREE = 12,
@@ -98,77 +104,6 @@ __host__ __device__ constexpr uint32_t p_offset(int hn, uint32_t row, uint32_t c
   return hn == 16 ? tc::sw32_offset(row, chunk) : hn == 32 ? tc::sw64_offset(row, chunk) : tc::sw128_offset(row, chunk);
 }
 
-// Walks a worker's (segment, page) sequence.
-struct Cursor {
-  int si, se, j;
-  Segment seg;
-  __device__ void begin(const DecodeArgs& a, int s0, int s1) {
-    si = s0; se = s1; j = 0;
-    if (si < se) seg = a.segs[si];
-  }
-  __device__ bool done() const { return si >= se; }
-  __device__ void next(const DecodeArgs& a) {
-    if (++j >= seg.num_pages) { j = 0; if (++si < se) seg = a.segs[si]; }
-  }
-  __device__ int valid() const { return min(kPage, seg.num_tokens - j * kPage); }
-  __device__ int64_t page(const DecodeArgs& a) const { return a.kv_indices[seg.page_begin + j]; }
-};
-
-__device__ __forceinline__ bool page_ok(const DecodeArgs& a, int64_t page) { return page >= 0 && page < a.num_pages; }
-
-// 32 bytes from global memory through the non-coherent path (the address must be 32-byte aligned).
-__device__ __forceinline__ void ldg_nc32(const void* p, uint32_t (&v)[8]) {
-  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-               : "l"(p));
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-struct Sync {
-  uint32_t bars;
-  volatile int* abort;
-  int* status;
-  __device__ uint32_t bar(uint32_t i) const { return bars + 8 * i; }
-  // Bounded wait for the phase of `parity`; on a timeout sets `code` in the status word and the abort
-  // flag (which ends every other wait of the CTA early).
-  __device__ bool wait(uint32_t i, uint32_t parity, int code) const {
-    const uint32_t b = bar(i);
-    if (tc::mbar_try_wait(b, parity)) return true;
-    const long long t0 = clock64();
-    for (int n = 0;; ++n) {
-      if (tc::mbar_try_wait_sleep(b, parity, kSleepNs)) return true;
-      if ((n & 255) == 0) {
-        if (*abort) return false;
-        if (clock64() - t0 > (1ll << 31)) {
-          *abort = 1;
-          atomicOr(status, code);
-          return false;
-        }
-      }
-    }
-  }
-};
-
-// Bounded wait until the counter at `addr` reaches `target` (acquire).
-__device__ bool wait_counter(const Sync& sy, uint32_t addr, uint32_t target) {
-  if (tc::ld_acquire_u32(addr) >= target) return true;
-  const long long t0 = clock64();
-  for (int n = 0;; ++n) {
-    if (tc::ld_acquire_u32(addr) >= target) return true;
-    if ((n & 255) == 0) {
-      if (*sy.abort) return false;
-      if (clock64() - t0 > (1ll << 31)) {
-        *sy.abort = 1;
-        atomicOr(sy.status, kStatusBase << 5);
-        return false;
-      }
-    }
-  }
-}
-
 // ---- dequantization of a page into an FP16 tile slot -------------------------------------------------
 // Tile: 9 atom columns (latent dims 64c .. 64c + 63), each 64 token rows of 128 bytes, 128-byte swizzle.
 template <int KV, int NT> struct Dequant;
@@ -202,7 +137,7 @@ template <int NT> struct Dequant<KV_FP8, NT> {
       const uint32_t at = tile + (q >> 7) * kColBytes;
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        sts128(at + tc::sw128_offset(tok, 4 * half + u), o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        sts128(at + tc::sw128_offset(tok, 4 * half + u), make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
     }
   }
 };
@@ -261,7 +196,7 @@ template <int NT> struct Dequant<KV_NVFP4, NT> {
       }
       const uint32_t at = tile + col * kColBytes;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sts128(at + tc::sw128_offset(tok, u), o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+      for (int u = 0; u < 8; ++u) sts128(at + tc::sw128_offset(tok, u), make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]));
     }
   }
 };
@@ -309,7 +244,7 @@ __device__ void role_dequant(const DecodeArgs& a, const Sync& sy, int seg_b, int
     if (nvalid > 0) D::load(rn, D::page_ptr(a, npg), nvalid, t);
     const int slot = g & 1;
     // slot last held page g - 2: its P.V completion frees it
-    if (g >= 2 && !sy.wait(B_T_EMPTY + slot, ((g >> 1) - 1) & 1, kStatusBase << 0)) return;
+    if (g >= 2 && !sy.wait(B_T_EMPTY + slot, ((g >> 1) - 1) & 1, false, kStatusBase << 0)) return;
     D::store(rc, valid, t, tiles + slot * kTileBytes);
     tc::fence_proxy_async_smem();
     tc::mbar_arrive(sy.bar(B_T_FULL + slot));
@@ -337,11 +272,11 @@ __device__ void role_qk(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_
   for (int g = 0; !cq.done(); ++g, cq.next(a)) {
     if (cq.j == 0 && cq.seg.req != q_req) { q_req = cq.seg.req; ++qcount; }
     const int slot = g & 1;
-    if (!sy.wait(B_T_FULL + slot, (g >> 1) & 1, kStatusBase << 1)) break;
+    if (!sy.wait(B_T_FULL + slot, (g >> 1) & 1, false, kStatusBase << 1)) break;
     // logit buffer `slot` was last read out for page g - 2
-    if (g >= 2 && !sy.wait(B_S_FREE + slot, ((g >> 1) - 1) & 1, kStatusBase << 1)) break;
+    if (g >= 2 && !sy.wait(B_S_FREE + slot, ((g >> 1) - 1) & 1, false, kStatusBase << 1)) break;
     if (q_waited != qcount) {
-      if (!wait_counter(sy, qver, static_cast<uint32_t>(qcount))) break;
+      if (!kern::wait_counter(sy, qver, static_cast<uint32_t>(qcount), kStatusBase << 5)) break;
       q_waited = qcount;
     }
     tc::tc_fence_after();
@@ -376,13 +311,13 @@ __device__ void role_pv(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_
   int si = 0;                                   // segments started
   for (int g = 0; !cp.done(); ++g) {
     const int pb = g % C::kPBufs;
-    if (!sy.wait(B_P_FULL + pb, (g / C::kPBufs) & 1, kStatusBase << 2)) break;
+    if (!sy.wait(B_P_FULL + pb, (g / C::kPBufs) & 1, false, kStatusBase << 2)) break;
     // already complete (Q.K^T of this page waited for it); the tile cannot be refilled before this P.V
-    if (!sy.wait(B_T_FULL + (g & 1), (g >> 1) & 1, kStatusBase << 2)) break;
+    if (!sy.wait(B_T_FULL + (g & 1), (g >> 1) & 1, false, kStatusBase << 2)) break;
     const bool first = cp.j == 0;
     if (first) {
       // O^T of the previous segment has been read out
-      if (si > 0 && !sy.wait(B_O_FREE, (si - 1) & 1, kStatusBase << 2)) break;
+      if (si > 0 && !sy.wait(B_O_FREE, (si - 1) & 1, false, kStatusBase << 2)) break;
       ++si;
     }
     tc::tc_fence_after();
@@ -442,7 +377,7 @@ struct SoftmaxSync {
   __device__ bool operator()(const Sync& sy) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) tc::mbar_arrive(bar);
-    const bool ok = sy.wait(B_SYNC, phase & 1, kStatusBase << 3);
+    const bool ok = sy.wait(B_SYNC, phase & 1, false, kStatusBase << 3);
     ++phase;
     return __all_sync(0xffffffffu, ok);
   }
@@ -478,8 +413,8 @@ __device__ void load_q(const DecodeArgs& a, int req, int tid, uint32_t qs, float
   for (int i = 0; i < kCpt; ++i) {
     const int chunk = part + kTpr * i;                 // 8 dims
     const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(qrow) + chunk) : make_uint4(0, 0, 0, 0);
-    sts128(qs + (chunk >> 3) * Cfg<HN>::kQCol + tc::sw128_offset(h, chunk & 7), dev::bf16x2_to_f16x2(v.x, down),
-           dev::bf16x2_to_f16x2(v.y, down), dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down));
+    sts128(qs + (chunk >> 3) * Cfg<HN>::kQCol + tc::sw128_offset(h, chunk & 7),
+           make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down), dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
   }
   if (part == 0) qsc[h] = sc;
 }
@@ -520,7 +455,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
   const uint32_t qs = base + C::OFF_Q, pbuf = base + C::OFF_P, qver = base + C::OFF_QVER;
   SoftmaxSync ssync{sy.bar(B_SYNC), 0};
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-    const bool ok = sy.wait(bar, parity, kStatusBase << 4);
+    const bool ok = sy.wait(bar, parity, false, kStatusBase << 4);
     return __all_sync(0xffffffffu, ok);
   };
   float lp[HN];                                    // this token's share of each head's row sum
@@ -660,7 +595,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
           lp[c0 + h8 + k + 1] += p1;
           pk[k / 2] = KV == KV_FP8PT ? dev::pack_f16x2(p0 * sig, p1 * sig) : dev::pack_f16x2(p0, p1);
         }
-        if (row_lane) sts128(prow + p_offset(HN, tok, (c0 + h8) / 8), pk[0], pk[1], pk[2], pk[3]);
+        if (row_lane) sts128(prow + p_offset(HN, tok, (c0 + h8) / 8), make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
     }
     tc::tc_fence_before();
@@ -783,7 +718,7 @@ __global__ void __launch_bounds__(Cfg<HN>::kThreads, 1) decode_tm_kernel(const D
     role_qk<HN>(a, sy, seg_b, seg_e, warp - C::kQkWarp0, tbase, base + C::OFF_T, base + C::OFF_Q, base + C::OFF_QVER);
   }
   // every MMA of the issuing threads has completed before TMEM is released
-  if (warp >= C::kPvWarp0 && (tid & 31) == 0) sy.wait(B_FINAL, 0, kStatusBase << 6);
+  if (warp >= C::kPvWarp0 && (tid & 31) == 0) sy.wait(B_FINAL, 0, false, kStatusBase << 6);
   __syncwarp();
   tc::tc_fence_before();
   __syncthreads();
