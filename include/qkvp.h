@@ -85,7 +85,7 @@ typedef enum {
   QKVP_ALGO_MMA_SYNC = 1,  /* warp-level mma.sync split-KV kernel, any supported head count */
   QKVP_ALGO_TCGEN05 = 2,   /* tcgen05/TMEM CTA-pair split-KV kernel: always 128 head rows (fewer heads
                               ride as zero rows), so its cost does not shrink with the heads; AUTO picks
-                              it at 64 heads and more, the mma.sync kernel below */
+                              it at 64 heads and more, and at 48 heads for FP8 and NVFP4 pools */
   QKVP_ALGO_MMA_FP8 = 3,   /* the mma.sync kernel with Q.K^T on the FP8 tensor-core path, for FP8 and
                               per-token-scaled FP8 pools (others: QKVP_E_UNSUPPORTED): K is the page's
                               E4M3 bytes as stored, Q is split per head row into two E4M3 terms,
@@ -103,10 +103,11 @@ typedef enum {
                               heads as the columns (N = 16, 32 or 64; 48 heads ride in 64): 16 to 64
                               heads, FP8, NVFP4 and per-token-scaled FP8 pools (others:
                               QKVP_E_UNSUPPORTED); one CTA per SM. Same arithmetic and tolerance as
-                              the other families. Measured on GB300 it is faster than AUTO's choice
-                              only for NVFP4 pools at 32 heads (10 x 160K: 479 us against 542 us);
-                              elsewhere slower (FP8 44 x 32K at 16 / 32 / 64 heads: 292 / 440 /
-                              918 us against 201 / 312 / 494 us), so AUTO never picks it. */
+                              the other families. Measured on GB300 it is the fastest family only for
+                              NVFP4 pools at 32 heads (10 x 160K: 479 us against 542 us for mma.sync;
+                              1M: 318 against 347 us), where AUTO picks it; elsewhere it is slower
+                              (FP8 44 x 32K at 16 / 32 / 64 heads: 292 / 440 / 918 us against
+                              201 / 312 / 494 us). */
 } qkvp_algo;
 
 #define QKVP_LATENT_DIM 576

@@ -80,6 +80,21 @@ int query_sms() {
 
 bool finite_float(float x) { return std::isfinite(x); }
 
+// The kernel family AUTO picks, from decode-kernel times measured on one GB300 (44 x 32K FP8,
+// 10 x 160K and 1 x 1M NVFP4, the 64-request mixed batch):
+// - The tcgen05 CTA-pair kernel always computes 128 head rows (fewer heads ride as zero rows), so it
+//   costs the same at any head count. For FP8 and NVFP4 pools it wins from 48 heads (48 heads:
+//   FP8 493 against 523 us for mma.sync, NVFP4 541 / 358 against 740 / 476 us); per-token-scaled FP8
+//   (48 heads: 588 against 537 us) and BF16 pools keep mma.sync below 64 heads.
+// - NVFP4 pools at 32 heads take the token-major tcgen05 kernel (479 / 318 us against 542 / 347 us).
+// - Everything else takes the mma.sync kernel, whose cost shrinks with the heads.
+int auto_algo(int num_heads, int kv_dtype) {
+  const bool plain = kv_dtype == QKVP_KV_FP8_E4M3 || kv_dtype == QKVP_KV_NVFP4;
+  if (num_heads >= 64 || (plain && num_heads >= 48)) return QKVP_ALGO_TCGEN05;
+  if (kv_dtype == QKVP_KV_NVFP4 && num_heads == 32) return QKVP_ALGO_TCGEN05_TOKENS;
+  return QKVP_ALGO_MMA_SYNC;
+}
+
 }  // namespace
 
 extern "C" {
@@ -128,11 +143,7 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   std::memset(plan, 0, sizeof(*plan));
   int st = check_plan_args(kv_indptr_host, kv_len_host, batch, num_heads, page_size, kv_dtype, min_splits);
   if (st != QKVP_OK) return st;
-  // The tcgen05 CTA-pair kernel always computes 128 head rows (fewer heads ride as zero rows), so it
-  // costs the same at any head count; below 64 heads the mma.sync kernel, whose cost shrinks with
-  // the heads, is faster (measured on the 44 x 32K FP8 workload: 16 heads 333 us, 32 heads 435 us,
-  // 64 heads 653 us, against ~560 us for the tcgen05 kernel).
-  if (algo == QKVP_ALGO_AUTO) algo = num_heads >= 64 ? QKVP_ALGO_TCGEN05 : QKVP_ALGO_MMA_SYNC;
+  if (algo == QKVP_ALGO_AUTO) algo = auto_algo(num_heads, kv_dtype);
   if (algo != QKVP_ALGO_MMA_SYNC && algo != QKVP_ALGO_TCGEN05 && algo != QKVP_ALGO_MMA_FP8 &&
       algo != QKVP_ALGO_TCGEN05_TOKENS)
     return QKVP_E_UNSUPPORTED;
