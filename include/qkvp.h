@@ -103,11 +103,10 @@ typedef enum {
                               heads as the columns (N = 16, 32 or 64; 48 heads ride in 64): 16 to 64
                               heads, FP8, NVFP4 and per-token-scaled FP8 pools (others:
                               QKVP_E_UNSUPPORTED); one CTA per SM. Same arithmetic and tolerance as
-                              the other families. Measured on GB300 it is the fastest family only for
-                              NVFP4 pools at 32 heads (10 x 160K: 479 us against 542 us for mma.sync;
-                              1M: 318 against 347 us), where AUTO picks it; elsewhere it is slower
-                              (FP8 44 x 32K at 16 / 32 / 64 heads: 292 / 440 / 918 us against
-                              201 / 312 / 494 us). */
+                              the other families. Measured on GB300: NVFP4 pools at 32 heads
+                              385 us (10 x 160K) and 241 us (1M) against 542 / 347 us for mma.sync, so
+                              AUTO picks it there; FP8 44 x 32K at 16 / 32 / 64 heads 278 / 333 / 488 us
+                              against 201 / 312 / 494 us for AUTO's choice. */
 } qkvp_algo;
 
 #define QKVP_LATENT_DIM 576

@@ -86,7 +86,7 @@ bool finite_float(float x) { return std::isfinite(x); }
 //   costs the same at any head count. For FP8 and NVFP4 pools it wins from 48 heads (48 heads:
 //   FP8 493 against 523 us for mma.sync, NVFP4 541 / 358 against 740 / 476 us); per-token-scaled FP8
 //   (48 heads: 588 against 537 us) and BF16 pools keep mma.sync below 64 heads.
-// - NVFP4 pools at 32 heads take the token-major tcgen05 kernel (479 / 318 us against 542 / 347 us).
+// - NVFP4 pools at 32 heads take the token-major tcgen05 kernel (385 / 241 us against 542 / 347 us).
 // - Everything else takes the mma.sync kernel, whose cost shrinks with the heads.
 int auto_algo(int num_heads, int kv_dtype) {
   const bool plain = kv_dtype == QKVP_KV_FP8_E4M3 || kv_dtype == QKVP_KV_NVFP4;

@@ -16,24 +16,24 @@
 // The page's dequantized FP16 tile (token rows of 64-dim atoms, 128-byte swizzle) is the K-major A
 // operand of the first product and, unchanged, the MN-major A operand of the second; Q (rows =
 // heads) and P (rows = tokens) are the B operands. The accumulator of an M = 64 product sits in TMEM
-// lanes 32 (r / 16) + r % 16 (measured), so softmax warp w holds tokens 16w .. 16w + 15 in its lanes
-// 0 .. 15, one token per thread with all HN logits in registers; O^T puts one output dim per TMEM lane.
+// lanes 32 (r / 16) + r % 16 (measured), so softmax warp w finds tokens 16w .. 16w + 15 in lanes 0 .. 15
+// of its quarter; the 16x256b load shape spreads them over all 32 threads (two tokens and a quarter of
+// the heads each). O^T puts one output dim per TMEM lane.
 //
-// Per CTA (512 threads, 384 for 64 heads; one CTA per SM, persistent over its worker's segments):
+// Per CTA (512 threads, one CTA per SM, persistent over its worker's segments):
 //   warps 0-3 (softmax): at a new request convert its Q rows to FP16 (rows holding |q| >= 2^15 are
-//     scaled by a power of two folded into the head's logit scale); per page read the token's HN
-//     logits, update the per-head running maxima lazily (only when a logit passes the maximum by more
-//     than 2^8, base 2; the decision is taken jointly by the four warps), rescale O^T and the row sums
-//     then, write the token's row of P; at a segment's end sum the row sums over the 64 tokens and
+//     scaled by a power of two folded into the head's logit scale); per page read the thread's logits,
+//     update the per-head running maxima lazily (only when a logit passes the maximum by more than 2^8,
+//     base 2; the decision is taken jointly by the four warps), rescale O^T and the row sums then,
+//     write the thread's words of P; at a segment's end sum the row sums over the 64 tokens and
 //     write O / l (or the normalised partial and its log2-sum-exp) from TMEM, one output dim per lane.
-//   warps 4-11 (4-8 for 64 heads; dequant): raw page bytes from global memory (32-byte loads, the next page's in flight
+//   warps 4-11 (dequant): raw page bytes from global memory (32-byte loads, the next page's in flight
 //     while the current one is written) into one of two FP16 tile slots; rows past the page's valid
 //     tokens are written as zeros.
 //   two Q.K^T warps: one thread each issues half of every page's 36 MMAs (latent dims 0-287 /
 //     288-575) into its own accumulator; the softmax adds the two in a fixed order. A thread waits
 //     ~50-70 cycles after each tcgen05.mma it issues, so two halves in flight halve the page's latency.
-//   two P.V warps: one thread each issues the MMAs of two of the four M-tiles of every page into O^T
-//     (64 heads: one thread, all four).
+//   two P.V warps: one thread each issues the MMAs of two of the four M-tiles of every page into O^T.
 // TMEM: logit buffers [page parity][K half] at [0, 4 HN), O^T [4 HN, 8 HN).
 // Every wait is bounded; a timeout sets bits in the status word and the CTA drains and exits.
 #include <cstdint>
@@ -89,11 +89,10 @@ struct Cfg {
   // logit buffers [page parity][K half], then O^T
   static constexpr uint32_t TM_S = 0, TM_O = 4 * HN;
   static_assert(8 * HN <= 512, "TMEM columns");
-  // Warps: 0-3 softmax, then the dequant warps, then one P.V, two Q.K^T and (up to 32 heads) a second
-  // P.V issuing warp. 16 warps leave 128 registers a thread; 64 heads keep 12 (168 registers) for the
-  // softmax's row sums, with 5 dequant warps and one P.V thread.
-  static constexpr int kPvThreads = HN == 64 ? 1 : 2;
-  static constexpr int kDqWarps = HN == 64 ? 5 : 8;
+  // Warps: 0-3 softmax, 4-11 dequant, then one P.V, two Q.K^T and a second P.V issuing warp; 16 warps
+  // leave 128 registers a thread.
+  static constexpr int kPvThreads = 2;
+  static constexpr int kDqWarps = 8;
   static constexpr int kDQ = 32 * kDqWarps;
   static constexpr int kPvWarp0 = 4 + kDqWarps, kQkWarp0 = kPvWarp0 + 1, kPvWarp1 = kPvWarp0 + 3;
   static constexpr int kThreads = 32 * (4 + kDqWarps + 2 + kPvThreads);
@@ -358,15 +357,32 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)
   else tc::tmem_st32(taddr, r);
 }
 
-// Element `lane` (0..3) of each 4-group of v[i0 .. i0 + 15], as a float4: a select chain instead of an
-// index that depends on the lane (which would put v in local memory).
+// 16 TMEM lanes x 8N columns, 16x256b shape: thread t of the warp gets lanes t / 4 and t / 4 + 8 of its
+// quarter and, of every 8-column group g, columns 8g + 2 (t % 4) and + 1: r[4g], r[4g + 1] from the
+// first lane, r[4g + 2], r[4g + 3] from the second (measured on the GPU).
 template <int N>
-__device__ __forceinline__ float4 lane_quad(const float (&v)[N], int i0, int lane) {
-  float4 r = make_float4(v[i0], v[i0 + 1], v[i0 + 2], v[i0 + 3]);
-#pragma unroll
-  for (int k = 1; k < 4; ++k)
-    if (lane == k) r = make_float4(v[i0 + 4 * k], v[i0 + 4 * k + 1], v[i0 + 4 * k + 2], v[i0 + 4 * k + 3]);
-  return r;
+__device__ __forceinline__ void tmem_ld_16x256(uint32_t taddr, uint32_t (&r)[4 * N]) {
+  static_assert(N == 2 || N == 4 || N == 8, "2, 4 or 8 column groups");
+  if constexpr (N == 2) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+  } else if constexpr (N == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+  } else {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+                   "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+  }
 }
 
 // Barrier of the four softmax warps: lane 0 of each warp arrives, every thread waits (bounded). All
@@ -419,22 +435,42 @@ __device__ void load_q(const DecodeArgs& a, int req, int tid, uint32_t qs, float
   if (part == 0) qsc[h] = sc;
 }
 
-// Scaled logits y = (S_lo + S_hi) * token scale * head scale of columns c0 .. c0 + CH - 1 of logit buffer s,
-// read from TMEM (-inf for rows that are not valid tokens). The softmax reads a buffer again rather
-// than holding it in registers: it cannot be refilled before the page's P.V has freed the tile anyway.
-template <int HN, int CH>
-__device__ __forceinline__ void logits(uint32_t tl, int s, int c0, bool live, float sig, const float* qsc, float (&y)[CH]) {
-  uint32_t ra[CH], rb[CH];
-  tmem_ld_cols<CH>(tl + Cfg<HN>::TM_S + (2 * s) * HN + c0, ra);
-  tmem_ld_cols<CH>(tl + Cfg<HN>::TM_S + (2 * s + 1) * HN + c0, rb);
+// Scaled logits y = (S_lo + S_hi) * token scale * head scale of this thread's two tokens and HN / 4
+// heads (16x256b layout: y[4g + k] token 0, y[4g + 2 + k] token 1, head 8g + hq + k), read from TMEM
+// (-inf for rows that are not valid tokens). The softmax reads a buffer again rather than holding it
+// in registers: it cannot be refilled before the page's P.V has freed the tile anyway.
+template <int HN>
+__device__ __forceinline__ void logits(uint32_t tl, int s, int hq, bool live0, bool live1, float sig0, float sig1,
+                                       const float* qsc, float (&y)[HN / 2]) {
+  uint32_t ra[HN / 2], rb[HN / 2];
+  tmem_ld_16x256<HN / 8>(tl + Cfg<HN>::TM_S + (2 * s) * HN, ra);
+  tmem_ld_16x256<HN / 8>(tl + Cfg<HN>::TM_S + (2 * s + 1) * HN, rb);
   tc::tmem_wait_ld();
 #pragma unroll
-  for (int u = 0; u < CH; u += 4) {
-    const float4 q4 = *reinterpret_cast<const float4*>(qsc + c0 + u);
-    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+  for (int g = 0; g < HN / 8; ++g) {
+    const float2 q2 = *reinterpret_cast<const float2*>(qsc + 8 * g + hq);
+    y[4 * g] = live0 ? (__uint_as_float(ra[4 * g]) + __uint_as_float(rb[4 * g])) * sig0 * q2.x : -INFINITY;
+    y[4 * g + 1] = live0 ? (__uint_as_float(ra[4 * g + 1]) + __uint_as_float(rb[4 * g + 1])) * sig0 * q2.y : -INFINITY;
+    y[4 * g + 2] = live1 ? (__uint_as_float(ra[4 * g + 2]) + __uint_as_float(rb[4 * g + 2])) * sig1 * q2.x : -INFINITY;
+    y[4 * g + 3] = live1 ? (__uint_as_float(ra[4 * g + 3]) + __uint_as_float(rb[4 * g + 3])) * sig1 * q2.y : -INFINITY;
+  }
+}
+
+// Per head of this thread, the reduction (max or sum) of v over the warp's 16 tokens: the 8 lane groups
+// with the same lane % 4 hold the same heads; lanes 0-3 then write the warp's values to red.
+template <int HN, bool kMax>
+__device__ __forceinline__ void warp_reduce_heads(float (&v)[HN / 4], float* red_w, int lane) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      y[u + k] = live ? (__uint_as_float(ra[u + k]) + __uint_as_float(rb[u + k])) * sig * qv[k] : -INFINITY;
+  for (int off = 4; off <= 16; off <<= 1)
+#pragma unroll
+    for (int i = 0; i < HN / 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], off);
+      v[i] = kMax ? fmaxf(v[i], o) : v[i] + o;
+    }
+  if (lane < 4) {
+#pragma unroll
+    for (int g = 0; g < HN / 8; ++g)
+      *reinterpret_cast<float2*>(red_w + 8 * g + 2 * lane) = make_float2(v[2 * g], v[2 * g + 1]);
   }
 }
 
@@ -442,10 +478,9 @@ template <int KV, int HN>
 __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int tid, uint32_t tbase,
                              uint32_t base, uint8_t* sbase) {
   using C = Cfg<HN>;
-  constexpr int CH = C::kChunk;
   const int w = tid >> 5, lane = tid & 31;
-  const bool row_lane = lane < 16;                // TMEM lanes 0..15 of the warp's quarter hold its tokens
-  const int tok = 16 * w + lane;
+  // this thread's tokens (rows of the warp's 16) and heads (2 of every 8-column group)
+  const int tok0 = 16 * w + (lane >> 2), tok1 = tok0 + 8, hq = 2 * (lane & 3);
   const uint32_t tl = tbase + (static_cast<uint32_t>(32 * w) << 16);
   float* m_run = reinterpret_cast<float*>(sbase + C::OFF_MRUN);
   float* qsc = reinterpret_cast<float*>(sbase + C::OFF_QSC);
@@ -458,22 +493,24 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
     const bool ok = sy.wait(bar, parity, false, kStatusBase << 4);
     return __all_sync(0xffffffffu, ok);
   };
-  float lp[HN];                                    // this token's share of each head's row sum
+  float lp[HN / 4];                                // this thread's two tokens' share of its heads' row sums
   Cursor cur;
   cur.begin(a, seg_b, seg_e);
   int cur_req = -1, nq = 0;
-  // the page index (and a per-token-scaled page's token scale) is read one page ahead
-  auto page_info = [&](const Cursor& c, int64_t& pg, int& valid, float& sig) {
-    pg = c.page(a);
+  // the page index (and a per-token-scaled page's token scales) is read one page ahead
+  auto page_info = [&](const Cursor& c, int& valid, float& s0, float& s1) {
+    const int64_t pg = c.page(a);
     valid = page_ok(a, pg) ? c.valid() : 0;
-    sig = 1.0f;
-    if (KV == KV_FP8PT && row_lane && tok < valid)
-      sig = __ldg(reinterpret_cast<const float*>(a.kv + pg * kPtPageBytes + kPtScaleOff) + tok);
+    s0 = s1 = 1.0f;
+    if (KV == KV_FP8PT) {
+      const float* sp = reinterpret_cast<const float*>(a.kv + pg * kPtPageBytes + kPtScaleOff);
+      if (tok0 < valid) s0 = __ldg(sp + tok0);
+      if (tok1 < valid) s1 = __ldg(sp + tok1);
+    }
   };
-  int64_t pg_n = 0;
   int valid_n = 0;
-  float sig_n = 1.0f;
-  if (!cur.done()) page_info(cur, pg_n, valid_n, sig_n);
+  float sig0_n = 1.0f, sig1_n = 1.0f;
+  if (!cur.done()) page_info(cur, valid_n, sig0_n, sig1_n);
   for (int g = 0; !cur.done(); ++g) {
     const Segment seg = cur.seg;
     if (cur.j == 0) {
@@ -487,7 +524,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       }
       if (tid < HN) m_run[tid] = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < HN; ++h) lp[h] = 0.0f;
+      for (int i = 0; i < HN / 4; ++i) lp[i] = 0.0f;
       if (!ssync(sy)) return;
       if (new_q) {
         ++nq;   // the Q.K^T threads count requests the same way
@@ -495,26 +532,26 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
       }
     }
     const int valid = valid_n;
-    const float sig = sig_n;
-    const bool live = row_lane && tok < valid;
+    const float sig0 = sig0_n, sig1 = sig1_n;
+    const bool live0 = tok0 < valid, live1 = tok1 < valid;
     {
       Cursor nx = cur;
       nx.next(a);
-      if (!nx.done()) page_info(nx, pg_n, valid_n, sig_n);
+      if (!nx.done()) page_info(nx, valid_n, sig0_n, sig1_n);
     }
     const int s = g & 1;
     if (!wait(B_S_FULL + s, (g >> 1) & 1)) return;
     tc::tc_fence_after();
     // ---- does any logit pass its head's running maximum by more than 2^8? (all four warps agree) ----
     bool flag = false;
+    {
+      float y[HN / 2];
+      logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
 #pragma unroll
-    for (int c0 = 0; c0 < HN; c0 += CH) {
-      float y[CH];
-      logits<HN, CH>(tl, s, c0, live, sig, qsc, y);
-#pragma unroll
-      for (int u = 0; u < CH; u += 4) {
-        const float4 m4 = *reinterpret_cast<const float4*>(m_run + c0 + u);
-        flag |= (y[u] > m4.x + 8.0f) | (y[u + 1] > m4.y + 8.0f) | (y[u + 2] > m4.z + 8.0f) | (y[u + 3] > m4.w + 8.0f);
+      for (int gg = 0; gg < HN / 8; ++gg) {
+        const float2 m2 = *reinterpret_cast<const float2*>(m_run + 8 * gg + hq);
+        flag |= (y[4 * gg] > m2.x + 8.0f) | (y[4 * gg + 1] > m2.y + 8.0f) | (y[4 * gg + 2] > m2.x + 8.0f) |
+                (y[4 * gg + 3] > m2.y + 8.0f);
       }
     }
     const bool wflag = __any_sync(0xffffffffu, flag);
@@ -522,21 +559,16 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
     if (!ssync(sy)) return;
     const int fp = ((ssync.phase - 1) & 1) * 4;
     if (flags[fp] | flags[fp + 1] | flags[fp + 2] | flags[fp + 3]) {
-      // the page's maximum of each head over its 64 tokens, then the renewed maxima (a rare path: kept
-      // rolled, the instruction cache holds the hot loop)
-#pragma unroll 1
-      for (int c0 = 0; c0 < HN; c0 += CH) {
-        float y[CH];
-        logits<HN, CH>(tl, s, c0, live, sig, qsc, y);
+      // the page's maximum of each head over its 64 tokens, then the renewed maxima
+      {
+        float y[HN / 2], mx[HN / 4];
+        logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
 #pragma unroll
-        for (int h0 = 0; h0 < CH; h0 += 16) {
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[h0 + i] = fmaxf(y[h0 + i], __shfl_xor_sync(0xffffffffu, y[h0 + i], off));
-          const float4 q4 = lane_quad(y, h0, lane);
-          if (lane < 4) *reinterpret_cast<float4*>(red + w * HN + c0 + h0 + 4 * lane) = q4;
+        for (int gg = 0; gg < HN / 8; ++gg) {
+          mx[2 * gg] = fmaxf(y[4 * gg], y[4 * gg + 2]);
+          mx[2 * gg + 1] = fmaxf(y[4 * gg + 1], y[4 * gg + 3]);
         }
+        warp_reduce_heads<HN, true>(mx, red + w * HN, lane);
       }
       if (!ssync(sy)) return;
       if (tid < HN) {
@@ -553,6 +585,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
         const int pq = (g - 1) % C::kPBufs;
         if (!wait(B_P_FREE + pq, ((g - 1) / C::kPBufs) & 1)) return;
         tc::tc_fence_after();
+        constexpr int CH = C::kChunk;
 #pragma unroll 1
         for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll 1
@@ -569,33 +602,33 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
         tc::tc_fence_before();
       }
 #pragma unroll
-      for (int h = 0; h < HN; h += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(alpha + h);
-        lp[h] *= a4.x; lp[h + 1] *= a4.y; lp[h + 2] *= a4.z; lp[h + 3] *= a4.w;
+      for (int gg = 0; gg < HN / 8; ++gg) {
+        const float2 a2 = *reinterpret_cast<const float2*>(alpha + 8 * gg + hq);
+        lp[2 * gg] *= a2.x;
+        lp[2 * gg + 1] *= a2.y;
       }
     }
-    // ---- P = 2^(y - m): this token's row, FP16 (per-token-scaled pages: times the token's scale) ----
+    // ---- P = 2^(y - m), FP16 (per-token-scaled pages: times the token's scale): each thread writes one
+    // 4-byte word (2 heads) per 8-head chunk of both its token rows ----
     const int pb = g % C::kPBufs;
     // P buffer pb was last read by PV(g - kPBufs)
     if (g >= C::kPBufs && !wait(B_P_FREE + pb, ((g / C::kPBufs) - 1) & 1)) return;
     const uint32_t prow = pbuf + pb * C::kPBytes;
+    {
+      float y[HN / 2];
+      logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
 #pragma unroll
-    for (int c0 = 0; c0 < HN; c0 += CH) {
-      float y[CH];
-      logits<HN, CH>(tl, s, c0, live, sig, qsc, y);
-#pragma unroll
-      for (int h8 = 0; h8 < CH; h8 += 8) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-          const float2 m2 = *reinterpret_cast<const float2*>(m_run + c0 + h8 + k);
-          const float p0 = dev::fast_exp2(y[h8 + k] - (m2.x == -INFINITY ? 0.0f : m2.x));
-          const float p1 = dev::fast_exp2(y[h8 + k + 1] - (m2.y == -INFINITY ? 0.0f : m2.y));
-          lp[c0 + h8 + k] += p0;
-          lp[c0 + h8 + k + 1] += p1;
-          pk[k / 2] = KV == KV_FP8PT ? dev::pack_f16x2(p0 * sig, p1 * sig) : dev::pack_f16x2(p0, p1);
-        }
-        if (row_lane) sts128(prow + p_offset(HN, tok, (c0 + h8) / 8), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+      for (int gg = 0; gg < HN / 8; ++gg) {
+        const float2 m2 = *reinterpret_cast<const float2*>(m_run + 8 * gg + hq);
+        const float mx = m2.x == -INFINITY ? 0.0f : m2.x, my = m2.y == -INFINITY ? 0.0f : m2.y;
+        const float p00 = dev::fast_exp2(y[4 * gg] - mx), p01 = dev::fast_exp2(y[4 * gg + 1] - my);
+        const float p10 = dev::fast_exp2(y[4 * gg + 2] - mx), p11 = dev::fast_exp2(y[4 * gg + 3] - my);
+        lp[2 * gg] += p00 + p10;
+        lp[2 * gg + 1] += p01 + p11;
+        const uint32_t w0 = KV == KV_FP8PT ? dev::pack_f16x2(p00 * sig0, p01 * sig0) : dev::pack_f16x2(p00, p01);
+        const uint32_t w1 = KV == KV_FP8PT ? dev::pack_f16x2(p10 * sig1, p11 * sig1) : dev::pack_f16x2(p10, p11);
+        tc::sts_u32(prow + p_offset(HN, tok0, gg) + 2 * hq, w0);
+        tc::sts_u32(prow + p_offset(HN, tok1, gg) + 2 * hq, w1);
       }
     }
     tc::tc_fence_before();
@@ -609,24 +642,14 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
     if (!last) continue;
 
     // ---- segment end: row sums over the 64 tokens (fixed order), then O / l from TMEM ----
-#pragma unroll
-    for (int h0 = 0; h0 < HN; h0 += 16) {
-      float t16[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) t16[i] = lp[h0 + i];
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) t16[i] += __shfl_xor_sync(0xffffffffu, t16[i], off);
-      const float4 q4 = lane_quad(t16, 0, lane);
-      if (lane < 4) *reinterpret_cast<float4*>(red + w * HN + h0 + 4 * lane) = q4;
-    }
+    warp_reduce_heads<HN, false>(lp, red + w * HN, lane);
     if (!ssync(sy)) return;
     if (tid < HN) alpha[tid] = (red[tid] + red[HN + tid]) + (red[2 * HN + tid] + red[3 * HN + tid]);
     if (!ssync(sy)) return;
     if (!wait(B_P_FREE + pb, (g / C::kPBufs) & 1)) return;     // PV(g) has completed
     tc::tc_fence_after();
     const int64_t row0 = static_cast<int64_t>(seg.req) * a.heads;
+    constexpr int CH = C::kChunk;
 #pragma unroll 1
     for (int mt = 0; mt < 4; ++mt) {
       const int dim = 128 * mt + 32 * w + lane;
