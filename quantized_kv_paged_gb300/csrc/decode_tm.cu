@@ -212,13 +212,15 @@ __device__ void role_dequant(const DecodeArgs& a, const Sync& sy, int seg_b, int
   Cursor cur;
   cur.begin(a, seg_b, seg_e);
   if (cur.done()) return;
-  typename D::Raw rc, rn;
+  // One register set: a page's raw loads are issued right after the previous page is written, so they
+  // land while the thread waits for the next tile slot (copying a second set would stall on them).
+  typename D::Raw rw;
   Cursor nx = cur;
   nx.next(a);
   int64_t npg = nx.done() ? 0 : nx.page(a);
   const int64_t pg0 = cur.page(a);
   int valid = page_ok(a, pg0) ? cur.valid() : 0;
-  if (valid > 0) D::load(rc, D::page_ptr(a, pg0), valid, t);
+  if (valid > 0) D::load(rw, D::page_ptr(a, pg0), valid, t);
   // one thread keeps the pages four ahead flowing into L2
   constexpr int kAhead = KV == KV_FP8 ? 4 : 0;
   Cursor pf = cur;
@@ -240,14 +242,13 @@ __device__ void role_dequant(const DecodeArgs& a, const Sync& sy, int seg_b, int
     if (!nn.done()) nn.next(a);
     const int64_t nnpg = nn.done() ? 0 : nn.page(a);
     const int nvalid = nx.done() ? 0 : (page_ok(a, npg) ? nx.valid() : 0);
-    if (nvalid > 0) D::load(rn, D::page_ptr(a, npg), nvalid, t);
     const int slot = g & 1;
     // slot last held page g - 2: its P.V completion frees it
     if (g >= 2 && !sy.wait(B_T_EMPTY + slot, ((g >> 1) - 1) & 1, false, kStatusBase << 0)) return;
-    D::store(rc, valid, t, tiles + slot * kTileBytes);
+    D::store(rw, valid, t, tiles + slot * kTileBytes);
     tc::fence_proxy_async_smem();
     tc::mbar_arrive(sy.bar(B_T_FULL + slot));
-    rc = rn;
+    if (nvalid > 0) D::load(rw, D::page_ptr(a, npg), nvalid, t);
     cur = nx;
     nx = nn;
     npg = nnpg;
