@@ -407,31 +407,57 @@ struct SoftmaxSync {
 template <int HN>
 __device__ void load_q(const DecodeArgs& a, int req, int tid, uint32_t qs, float* qsc) {
   constexpr int kTpr = 128 / HN, kChunks = kLatent / 8, kCpt = kChunks / kTpr;
+  constexpr int kBatch = 9;                          // 16-byte loads in flight per thread
+  static_assert(kCpt % kBatch == 0, "batches of chunks");
   const int h = tid / kTpr, part = tid % kTpr;
   const bool live = h < a.heads;
-  const uint8_t* qrow = reinterpret_cast<const uint8_t*>(a.q) + (static_cast<int64_t>(req) * a.heads + (live ? h : 0)) * (kLatent * 2);
-  uint32_t mx = 0;
+  const uint4* qrow = reinterpret_cast<const uint4*>(a.q) + (static_cast<int64_t>(req) * a.heads + (live ? h : 0)) * (kLatent / 8);
+  auto big = [](uint32_t w) { return (w & 0x7FFFu) >= 0x4700u || ((w >> 16) & 0x7FFFu) >= 0x4700u; };
+  // the row unscaled, in batches of loads in flight; a value of 2^15 or more (or inf / NaN) makes the
+  // row convert again below with a power-of-two scale
+  bool hot = false;
 #pragma unroll 1
-  for (int i = 0; i < kCpt; ++i) {
-    const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(qrow) + part + kTpr * i) : make_uint4(0, 0, 0, 0);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int i0 = 0; i0 < kCpt; i0 += kBatch) {
+    uint4 v[kBatch];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
-  }
+    for (int i = 0; i < kBatch; ++i) v[i] = live ? __ldg(qrow + part + kTpr * (i0 + i)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-  for (int off = 1; off < kTpr; off <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  float down = 1.0f, sc = a.scale_log2;
-  if (mx >= 0x4700u && mx < 0x7F80u) {
-    const int sh = max(-100, min(113, static_cast<int>(mx >> 7) - 127 - 14));
-    down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-    sc = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+    for (int i = 0; i < kBatch; ++i) {
+      const int chunk = part + kTpr * (i0 + i);         // 8 dims
+      hot |= big(v[i].x) || big(v[i].y) || big(v[i].z) || big(v[i].w);
+      sts128(qs + (chunk >> 3) * Cfg<HN>::kQCol + tc::sw128_offset(h, chunk & 7),
+             make_uint4(dev::bf16x2_to_f16x2(v[i].x), dev::bf16x2_to_f16x2(v[i].y), dev::bf16x2_to_f16x2(v[i].z),
+                        dev::bf16x2_to_f16x2(v[i].w)));
+    }
   }
+  // the kTpr threads of a row agree (aligned groups of consecutive lanes)
+#pragma unroll
+  for (int off = 1; off < kTpr; off <<= 1) hot |= __shfl_xor_sync(0xffffffffu, hot ? 1 : 0, off) != 0;
+  float sc = a.scale_log2;
+  if (__any_sync(0xffffffffu, hot) && hot) {
+    uint32_t mx = 0;
 #pragma unroll 1
-  for (int i = 0; i < kCpt; ++i) {
-    const int chunk = part + kTpr * i;                 // 8 dims
-    const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(qrow) + chunk) : make_uint4(0, 0, 0, 0);
-    sts128(qs + (chunk >> 3) * Cfg<HN>::kQCol + tc::sw128_offset(h, chunk & 7),
-           make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down), dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
+    for (int i = 0; i < kCpt; ++i) {
+      const uint4 v = __ldg(qrow + part + kTpr * i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int off = 1; off < kTpr; off <<= 1) mx = max(mx, __shfl_xor_sync(__activemask(), mx, off));
+    if (mx < 0x7F80u) {                               // inf / NaN rows stay unscaled
+      const int sh = max(-100, min(113, static_cast<int>(mx >> 7) - 127 - 14));
+      const float down = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+      sc = a.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+#pragma unroll 1
+      for (int i = 0; i < kCpt; ++i) {
+        const int chunk = part + kTpr * i;
+        const uint4 v = __ldg(qrow + chunk);
+        sts128(qs + (chunk >> 3) * Cfg<HN>::kQCol + tc::sw128_offset(h, chunk & 7),
+               make_uint4(dev::bf16x2_to_f16x2(v.x, down), dev::bf16x2_to_f16x2(v.y, down),
+                          dev::bf16x2_to_f16x2(v.z, down), dev::bf16x2_to_f16x2(v.w, down)));
+      }
+    }
   }
   if (part == 0) qsc[h] = sc;
 }
