@@ -85,7 +85,7 @@ typedef enum {
   QKVP_ALGO_MMA_SYNC = 1,  /* warp-level mma.sync split-KV kernel, any supported head count */
   QKVP_ALGO_TCGEN05 = 2,   /* tcgen05/TMEM CTA-pair split-KV kernel: always 128 head rows (fewer heads
                               ride as zero rows), so its cost does not shrink with the heads; AUTO picks
-                              it at 64 heads and more, and at 48 heads for FP8 and NVFP4 pools */
+                              it above 64 heads (from 64 for BF16 pools) */
   QKVP_ALGO_MMA_FP8 = 3,   /* the mma.sync kernel with Q.K^T on the FP8 tensor-core path, for FP8 and
                               per-token-scaled FP8 pools (others: QKVP_E_UNSUPPORTED): K is the page's
                               E4M3 bytes as stored, Q is split per head row into two E4M3 terms,
@@ -103,10 +103,11 @@ typedef enum {
                               heads as the columns (N = 16, 32 or 64; 48 heads ride in 64): 16 to 64
                               heads, FP8, NVFP4 and per-token-scaled FP8 pools (others:
                               QKVP_E_UNSUPPORTED); one CTA per SM. Same arithmetic and tolerance as
-                              the other families. Measured on GB300: NVFP4 pools at 32 heads
-                              385 us (10 x 160K) and 241 us (1M) against 542 / 347 us for mma.sync, so
-                              AUTO picks it there; FP8 44 x 32K at 16 / 32 / 64 heads 278 / 333 / 488 us
-                              against 201 / 312 / 494 us for AUTO's choice. */
+                              the other families. AUTO picks it for quantized pools at 32 to 64 heads,
+                              where it measured fastest on GB300 (FP8 44 x 32K at 32 / 64 heads:
+                              292 / 476 us against 311 / 495 us for the other families; NVFP4 1M:
+                              237 / 328 against 347 / 361 us). At 16 heads the mma.sync kernel is
+                              faster. */
 } qkvp_algo;
 
 #define QKVP_LATENT_DIM 576

@@ -18,6 +18,10 @@ namespace {
 
 constexpr uint64_t kAlign = kTableAlign;
 constexpr int kTcSegmentCost = 14;  // pages of work one request start costs the tcgen05 kernel
+// ... and the token-major tcgen05 kernel (its pipeline drains at a request's Q load and segment end;
+// measured on the 64-request mixed batch at 16 / 32 / 64 heads: no charge 119 / 163 / 265 us, 8 pages
+// 98 / 124 / 206 us, 20 pages 103 / 122 / 183 us)
+constexpr int kTmSegmentCost = 20;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -80,18 +84,20 @@ int query_sms() {
 
 bool finite_float(float x) { return std::isfinite(x); }
 
-// The kernel family AUTO picks, from decode-kernel times measured on one GB300 (44 x 32K FP8,
-// 10 x 160K and 1 x 1M NVFP4, the 64-request mixed batch):
-// - The tcgen05 CTA-pair kernel always computes 128 head rows (fewer heads ride as zero rows), so it
-//   costs the same at any head count. For FP8 and NVFP4 pools it wins from 48 heads (48 heads:
-//   FP8 493 against 523 us for mma.sync, NVFP4 541 / 358 against 740 / 476 us); per-token-scaled FP8
-//   (48 heads: 588 against 537 us) and BF16 pools keep mma.sync below 64 heads.
-// - NVFP4 pools at 32 heads take the token-major tcgen05 kernel (385 / 241 us against 542 / 347 us).
-// - Everything else takes the mma.sync kernel, whose cost shrinks with the heads.
+// The kernel family AUTO picks, from decode-kernel times measured on one GB300 (44 x 32K FP8 and
+// per-token FP8, 10 x 160K and 1 x 1M NVFP4, the 64-request mixed batch; decode kernel only):
+// - 32 to 64 heads on quantized pools: the token-major tcgen05 kernel. FP8 at 32 / 48 / 64 heads
+//   292 / 393 / 476 us against 311 (mma.sync) / 494 / 495 us (CTA pair); per-token FP8 298 / 459 /
+//   474 against 322 / 539 / 542 us (mma.sync); NVFP4 10 x 160K at 32 / 64 heads 373 / 476 against 542
+//   (mma.sync) / 544 us, 1M 237 / 328 against 347 / 361 us; mixed batch at 32 / 48 / 64 heads
+//   122 / 173 / 183 against 123 / 183 / 185 us.
+// - 16 heads: the mma.sync kernel (FP8 200 against 273 us, NVFP4 277 against 335 us, mixed batch 90
+//   against 103 us).
+// - More heads (and BF16 pools from 64): the tcgen05 CTA-pair kernel, whose 128 head rows cost the
+//   same at any head count; BF16 pools below 64 heads take mma.sync.
 int auto_algo(int num_heads, int kv_dtype) {
-  const bool plain = kv_dtype == QKVP_KV_FP8_E4M3 || kv_dtype == QKVP_KV_NVFP4;
-  if (num_heads >= 64 || (plain && num_heads >= 48)) return QKVP_ALGO_TCGEN05;
-  if (kv_dtype == QKVP_KV_NVFP4 && num_heads == 32) return QKVP_ALGO_TCGEN05_TOKENS;
+  if (kv_dtype != QKVP_KV_BF16 && num_heads >= 32 && num_heads <= 64) return QKVP_ALGO_TCGEN05_TOKENS;
+  if (num_heads >= 64) return QKVP_ALGO_TCGEN05;
   return QKVP_ALGO_MMA_SYNC;
 }
 
@@ -188,7 +194,9 @@ int mla_decode_plan(const int32_t* kv_indptr_host, const int32_t* kv_len_host, i
   // baseline) take about three times longer per page, so a request start costs them little and equal
   // quotas balance better (mixed batch 500 us against 522 us with the charge); the mma.sync kernel's
   // split gives equal page quotas too.
-  const int seg_cost = algo == QKVP_ALGO_TCGEN05 && kv_dtype != QKVP_KV_BF16 ? kTcSegmentCost : 0;
+  const int seg_cost = algo == QKVP_ALGO_TCGEN05 && kv_dtype != QKVP_KV_BF16 ? kTcSegmentCost
+                       : algo == QKVP_ALGO_TCGEN05_TOKENS                     ? kTmSegmentCost
+                                                                              : 0;
   // count the segments, then fill the table arrays
   SplitInfo info;
   split_pages(kv_indptr_host, kv_len_host, batch, workers, min_splits, SplitOut{}, info, seg_cost);

@@ -58,18 +58,17 @@ def test_plan_rejects_bad_arguments(lib):
     assert plan(np.array([0, 2, 1], np.int32), np.array([5, 5], np.int32)).status == q.QKVP_E_INVALID
     assert plan(ok_ptr, ok_len, min_splits=-1).status == q.QKVP_E_INVALID
     assert plan(ok_ptr, ok_len, algo=7).status == q.QKVP_E_UNSUPPORTED
-    # AUTO: the tcgen05 kernel from 64 heads up (it always computes 128 head rows) and from 48 for FP8
-    # and NVFP4 pools; NVFP4 at 32 heads the token-major kernel; mma.sync otherwise
-    assert plan(ok_ptr, ok_len, heads=64).algo == q.ALGO_TCGEN05
-    for kv in (q.KV_FP8_E4M3, q.KV_NVFP4):
-        assert plan(ok_ptr, ok_len, heads=48, kv=kv).algo == q.ALGO_TCGEN05
-    for kv in (q.KV_FP8_PER_TOKEN, q.KV_BF16):
-        assert plan(ok_ptr, ok_len, heads=48, kv=kv).algo == q.ALGO_MMA_SYNC
-        assert plan(ok_ptr, ok_len, heads=64, kv=kv).algo == q.ALGO_TCGEN05
-    assert plan(ok_ptr, ok_len, heads=32, kv=q.KV_NVFP4).algo == q.ALGO_TCGEN05_TOKENS
-    for kv in (q.KV_FP8_E4M3, q.KV_FP8_PER_TOKEN, q.KV_BF16):
-        assert plan(ok_ptr, ok_len, heads=32, kv=kv).algo == q.ALGO_MMA_SYNC
-    assert plan(ok_ptr, ok_len, heads=16, kv=q.KV_NVFP4).algo == q.ALGO_MMA_SYNC
+    # AUTO: quantized pools take the token-major kernel at 32-64 heads, mma.sync at 16, the tcgen05
+    # CTA-pair kernel above 64; BF16 pools mma.sync below 64 heads, the CTA-pair kernel from 64
+    for kv in (q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_FP8_PER_TOKEN):
+        assert plan(ok_ptr, ok_len, heads=16, kv=kv).algo == q.ALGO_MMA_SYNC
+        for heads in (32, 48, 64):
+            assert plan(ok_ptr, ok_len, heads=heads, kv=kv).algo == q.ALGO_TCGEN05_TOKENS
+        for heads in (80, 128):
+            assert plan(ok_ptr, ok_len, heads=heads, kv=kv).algo == q.ALGO_TCGEN05
+    for heads in (16, 32, 48):
+        assert plan(ok_ptr, ok_len, heads=heads, kv=q.KV_BF16).algo == q.ALGO_MMA_SYNC
+    assert plan(ok_ptr, ok_len, heads=64, kv=q.KV_BF16).algo == q.ALGO_TCGEN05
     assert plan(ok_ptr, ok_len, heads=16, algo=q.ALGO_TCGEN05).status == q.QKVP_OK
 
 
@@ -252,7 +251,7 @@ def test_fp8_qk_algo_plans_fp8_pools_only(lib):
 
 def test_token_major_algo_plans_16_to_64_heads(lib):
     """QKVP_ALGO_TCGEN05_TOKENS: one CTA per SM (workers = SMs, one CTA each), 16-64 heads, quantized
-    pools only; AUTO picks it only for NVFP4 pools at 32 heads."""
+    pools only."""
     ptr, lens = np.array([0, 2], np.int32), np.array([100], np.int32)
     for kv in (q.KV_FP8_E4M3, q.KV_NVFP4, q.KV_FP8_PER_TOKEN):
         for heads in (16, 32, 48, 64):
@@ -262,5 +261,4 @@ def test_token_major_algo_plans_16_to_64_heads(lib):
         for heads in (80, 128):
             assert plan(ptr, lens, heads=heads, kv=kv, algo=q.ALGO_TCGEN05_TOKENS).status == q.QKVP_E_UNSUPPORTED
     assert plan(ptr, lens, heads=32, kv=q.KV_BF16, algo=q.ALGO_TCGEN05_TOKENS).status == q.QKVP_E_UNSUPPORTED
-    for heads in (16, 32, 64):
-        assert plan(ptr, lens, heads=heads).algo != q.ALGO_TCGEN05_TOKENS     # FP8 pools
+    assert plan(ptr, lens, heads=16).algo != q.ALGO_TCGEN05_TOKENS
