@@ -69,6 +69,7 @@ struct Cfg {
   static constexpr uint32_t kPRow = HN * 2;             // P row of one token: HN FP16
   static constexpr uint32_t kPBytes = kPage * kPRow;
   static constexpr int kPBufs = HN == 64 ? 1 : 2;       // 64 heads: shared memory holds one P buffer
+  static constexpr bool kSpecP = HN <= 32;              // P before the maxima agreement (see role_softmax)
   static constexpr uint32_t kPSwizzle = HN == 16 ? tc::kSwizzle32 : HN == 32 ? tc::kSwizzle64 : tc::kSwizzle128;
   static constexpr uint32_t OFF_T = 0;
   static constexpr uint32_t OFF_Q = OFF_T + 2 * kTileBytes;
@@ -569,24 +570,19 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
     const int s = g & 1;
     if (!wait(B_S_FULL + s, (g >> 1) & 1)) return;
     tc::tc_fence_after();
-    // ---- does any logit pass its head's running maximum by more than 2^8? (all four warps agree) ----
-    bool flag = false;
-    {
-      float y[HN / 2];
-      logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
-#pragma unroll
-      for (int gg = 0; gg < HN / 8; ++gg) {
-        const float2 m2 = *reinterpret_cast<const float2*>(m_run + 8 * gg + hq);
-        flag |= (y[4 * gg] > m2.x + 8.0f) | (y[4 * gg + 1] > m2.y + 8.0f) | (y[4 * gg + 2] > m2.x + 8.0f) |
-                (y[4 * gg + 3] > m2.y + 8.0f);
-      }
-    }
-    const bool wflag = __any_sync(0xffffffffu, flag);
-    if (lane == 0) flags[(ssync.phase & 1) * 4 + w] = wflag ? 1 : 0;
-    if (!ssync(sy)) return;
-    const int fp = ((ssync.phase - 1) & 1) * 4;
-    if (flags[fp] | flags[fp + 1] | flags[fp + 2] | flags[fp + 3]) {
-      // the page's maximum of each head over its 64 tokens, then the renewed maxima
+    const int pb = g % C::kPBufs;
+    const uint32_t prow = pbuf + pb * C::kPBytes;
+    // the four warps agree whether any logit passes its head's running maximum by more than 2^8
+    auto agree = [&](bool flag) -> int {
+      const bool wflag = __any_sync(0xffffffffu, flag);
+      if (lane == 0) flags[(ssync.phase & 1) * 4 + w] = wflag ? 1 : 0;
+      if (!ssync(sy)) return -1;
+      const int fp = ((ssync.phase - 1) & 1) * 4;
+      return (flags[fp] | flags[fp + 1] | flags[fp + 2] | flags[fp + 3]) ? 1 : 0;
+    };
+    // the page's maximum of each head over its 64 tokens, the renewed maxima (and, in red, the ones
+    // they replace), and O^T's head columns rescaled
+    auto renew_maxima = [&]() -> bool {
       {
         float y[HN / 2], mx[HN / 4];
         logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
@@ -597,7 +593,7 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
         }
         warp_reduce_heads<HN, true>(mx, red + w * HN, lane);
       }
-      if (!ssync(sy)) return;
+      if (!ssync(sy)) return false;
       if (tid < HN) {
         const float pm = fmaxf(fmaxf(red[tid], red[HN + tid]), fmaxf(red[2 * HN + tid], red[3 * HN + tid]));
         const float mo = m_run[tid];
@@ -605,12 +601,13 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
         const float mn = renew ? pm : mo;
         alpha[tid] = renew ? dev::fast_exp2(mo - mn) : 1.0f;   // 0 when mo is -inf
         m_run[tid] = mn;
+        if (C::kSpecP) red[tid] = mo;
       }
-      if (!ssync(sy)) return;
+      if (!ssync(sy)) return false;
       if (cur.j > 0) {
         // O^T holds this segment's earlier pages: rescale its head columns once PV(g - 1) has completed
         const int pq = (g - 1) % C::kPBufs;
-        if (!wait(B_P_FREE + pq, ((g - 1) / C::kPBufs) & 1)) return;
+        if (!wait(B_P_FREE + pq, ((g - 1) / C::kPBufs) & 1)) return false;
         tc::tc_fence_after();
         constexpr int CH = C::kChunk;
 #pragma unroll 1
@@ -628,20 +625,102 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
         tc::tmem_wait_st();
         tc::tc_fence_before();
       }
-#pragma unroll
-      for (int gg = 0; gg < HN / 8; ++gg) {
-        const float2 a2 = *reinterpret_cast<const float2*>(alpha + 8 * gg + hq);
-        lp[2 * gg] *= a2.x;
-        lp[2 * gg + 1] *= a2.y;
-      }
-    }
-    // ---- P = 2^(y - m), FP16 (per-token-scaled pages: times the token's scale): each thread writes one
-    // 4-byte word (2 heads) per 8-head chunk of both its token rows ----
-    const int pb = g % C::kPBufs;
+      return true;
+    };
     // P buffer pb was last read by PV(g - kPBufs)
-    if (g >= C::kPBufs && !wait(B_P_FREE + pb, ((g / C::kPBufs) - 1) & 1)) return;
-    const uint32_t prow = pbuf + pb * C::kPBytes;
-    {
+    const bool pfree_wait = g >= C::kPBufs;
+    const uint32_t pfree_par = ((g / C::kPBufs) - 1) & 1;
+    if constexpr (C::kSpecP) {
+      // ---- up to 32 heads, P = 2^(y - m) at once against the current maxima, FP16 (per-token-scaled
+      // pages: times the token's scale), one 4-byte word (two heads) per token and 8-head chunk,
+      // stored once the buffer is free. A logit that passes its maximum by more than 2^8 keeps its p
+      // out of the row sum and has the maxima renewed and P taken again. ----
+      bool flag = false;
+      uint32_t pw[HN / 4];
+      {
+        float y[HN / 2];
+        logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
+#pragma unroll
+        for (int gg = 0; gg < HN / 8; ++gg) {
+          const float2 m2 = *reinterpret_cast<const float2*>(m_run + 8 * gg + hq);
+          const float mx = m2.x == -INFINITY ? 0.0f : m2.x, my = m2.y == -INFINITY ? 0.0f : m2.y;
+          const float p00 = dev::fast_exp2(y[4 * gg] - mx), p01 = dev::fast_exp2(y[4 * gg + 1] - my);
+          const float p10 = dev::fast_exp2(y[4 * gg + 2] - mx), p11 = dev::fast_exp2(y[4 * gg + 3] - my);
+          const bool k00 = !(y[4 * gg] > m2.x + 8.0f), k01 = !(y[4 * gg + 1] > m2.y + 8.0f);
+          const bool k10 = !(y[4 * gg + 2] > m2.x + 8.0f), k11 = !(y[4 * gg + 3] > m2.y + 8.0f);
+          flag |= !(k00 && k01 && k10 && k11);
+          lp[2 * gg] += (k00 ? p00 : 0.0f) + (k10 ? p10 : 0.0f);
+          lp[2 * gg + 1] += (k01 ? p01 : 0.0f) + (k11 ? p11 : 0.0f);
+          pw[2 * gg] = KV == KV_FP8PT ? dev::pack_f16x2(p00 * sig0, p01 * sig0) : dev::pack_f16x2(p00, p01);
+          pw[2 * gg + 1] = KV == KV_FP8PT ? dev::pack_f16x2(p10 * sig1, p11 * sig1) : dev::pack_f16x2(p10, p11);
+        }
+      }
+      const int any = agree(flag);
+      if (any < 0) return;
+      if (!any) {
+        if (pfree_wait && !wait(B_P_FREE + pb, pfree_par)) return;
+#pragma unroll
+        for (int gg = 0; gg < HN / 8; ++gg) {
+          tc::sts_u32(prow + p_offset(HN, tok0, gg) + 2 * hq, pw[2 * gg]);
+          tc::sts_u32(prow + p_offset(HN, tok1, gg) + 2 * hq, pw[2 * gg + 1]);
+        }
+      } else {
+        if (!renew_maxima()) return;
+        if (pfree_wait && !wait(B_P_FREE + pb, pfree_par)) return;
+        // P against the renewed maxima; a renewed head's row sums drop the terms the first P gave
+        // them, are rescaled, and take the new ones
+        float y[HN / 2];
+        logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
+#pragma unroll
+        for (int gg = 0; gg < HN / 8; ++gg) {
+          float pn[4];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int h = 8 * gg + hq + k;
+            const float mo = red[h], mn = m_run[h], al = alpha[h];
+            const float mref = mn == -INFINITY ? 0.0f : mn;
+            pn[k] = dev::fast_exp2(y[4 * gg + k] - mref);
+            pn[2 + k] = dev::fast_exp2(y[4 * gg + 2 + k] - mref);
+            if (!(mn == mo)) {
+              const float moref = mo == -INFINITY ? 0.0f : mo;
+              const float po0 = !(y[4 * gg + k] > mo + 8.0f) ? dev::fast_exp2(y[4 * gg + k] - moref) : 0.0f;
+              const float po1 = !(y[4 * gg + 2 + k] > mo + 8.0f) ? dev::fast_exp2(y[4 * gg + 2 + k] - moref) : 0.0f;
+              lp[2 * gg + k] = al * (lp[2 * gg + k] - po0 - po1) + pn[k] + pn[2 + k];
+            }
+          }
+          const uint32_t w0 = KV == KV_FP8PT ? dev::pack_f16x2(pn[0] * sig0, pn[1] * sig0) : dev::pack_f16x2(pn[0], pn[1]);
+          const uint32_t w1 = KV == KV_FP8PT ? dev::pack_f16x2(pn[2] * sig1, pn[3] * sig1) : dev::pack_f16x2(pn[2], pn[3]);
+          tc::sts_u32(prow + p_offset(HN, tok0, gg) + 2 * hq, w0);
+          tc::sts_u32(prow + p_offset(HN, tok1, gg) + 2 * hq, w1);
+        }
+      }
+    } else {
+      // ---- from 48 heads (one P buffer), the agreement first ----
+      bool flag = false;
+      {
+        float y[HN / 2];
+        logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
+#pragma unroll
+        for (int gg = 0; gg < HN / 8; ++gg) {
+          const float2 m2 = *reinterpret_cast<const float2*>(m_run + 8 * gg + hq);
+          flag |= (y[4 * gg] > m2.x + 8.0f) | (y[4 * gg + 1] > m2.y + 8.0f) | (y[4 * gg + 2] > m2.x + 8.0f) |
+                  (y[4 * gg + 3] > m2.y + 8.0f);
+        }
+      }
+      const int any = agree(flag);
+      if (any < 0) return;
+      if (any) {
+        if (!renew_maxima()) return;
+#pragma unroll
+        for (int gg = 0; gg < HN / 8; ++gg) {
+          const float2 a2 = *reinterpret_cast<const float2*>(alpha + 8 * gg + hq);
+          lp[2 * gg] *= a2.x;
+          lp[2 * gg + 1] *= a2.y;
+        }
+      }
+      // ---- P = 2^(y - m), FP16 (per-token-scaled pages: times the token's scale): each thread writes
+      // one 4-byte word (2 heads) per 8-head chunk of both its token rows ----
+      if (pfree_wait && !wait(B_P_FREE + pb, pfree_par)) return;
       float y[HN / 2];
       logits<HN>(tl, s, hq, live0, live1, sig0, sig1, qsc, y);
 #pragma unroll
