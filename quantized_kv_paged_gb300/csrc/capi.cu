@@ -87,12 +87,12 @@ bool finite_float(float x) { return std::isfinite(x); }
 // The kernel family AUTO picks, from decode-kernel times measured on one GB300 (44 x 32K FP8 and
 // per-token FP8, 10 x 160K and 1 x 1M NVFP4, the 64-request mixed batch; decode kernel only):
 // - 32 to 64 heads on quantized pools: the token-major tcgen05 kernel. FP8 at 32 / 48 / 64 heads
-//   292 / 393 / 476 us against 311 (mma.sync) / 494 / 495 us (CTA pair); per-token FP8 298 / 459 /
-//   474 against 322 / 539 / 542 us (mma.sync); NVFP4 10 x 160K at 32 / 64 heads 373 / 476 against 542
-//   (mma.sync) / 544 us, 1M 237 / 328 against 347 / 361 us; mixed batch at 32 / 48 / 64 heads
-//   122 / 173 / 183 against 123 / 183 / 185 us.
-// - 16 heads: the mma.sync kernel (FP8 200 against 273 us, NVFP4 277 against 335 us, mixed batch 90
-//   against 103 us).
+//   291 / 390 / 405 us against 311 (mma.sync) / 494 / 495 us (CTA pair); per-token FP8 296 / 459 /
+//   474 against 322 / 539 / 542 us (mma.sync); NVFP4 10 x 160K at 32 / 64 heads 350 / 484 against 542
+//   (mma.sync) / 544 us, 1M 236 / 333 against 347 / 361 us; mixed batch at 32 / 48 / 64 heads
+//   124 / 173 / 182 against 123 / 183 / 185 us.
+// - 16 heads: the mma.sync kernel (FP8 200 against 255 us, NVFP4 279 against 313 us, mixed batch 91
+//   against 101 us).
 // - More heads (and BF16 pools from 64): the tcgen05 CTA-pair kernel, whose 128 head rows cost the
 //   same at any head count; BF16 pools below 64 heads take mma.sync.
 int auto_algo(int num_heads, int kv_dtype) {
