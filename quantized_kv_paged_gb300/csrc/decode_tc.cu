@@ -73,8 +73,9 @@ constexpr uint32_t kAtom = 4096;             // 32 token rows x 64 dims FP16, 12
 // and of the other 32 tokens (P.V only): 8 atoms, freed when P.V completes.
 constexpr int kKSlots = 2, kVSlots = 3;
 // Pages ahead that the dequant role prefetches into L2. Measured on one GB300: FP8 pools gain (44 x 32K:
-// 547 -> 539 us); pools whose dequant warps do more per byte lose (NVFP4 10 x 160K: 724 -> 747 us,
-// per-token-scaled FP8 44 x 32K: 635 -> 679 us), and BF16 pools are unchanged. So FP8 only.
+// 515 -> 507 us); NVFP4 pools lose (10 x 160K: 724 -> 747 us), per-token-scaled FP8 pools too (44 x
+// 32K: 584 -> 607 us four pages ahead, 617 us two ahead, the token rows alone or with their scales),
+// and BF16 pools are unchanged. So FP8 only.
 template <int KV>
 constexpr int prefetch_ahead() { return KV == KV_FP8 ? 4 : 0; }
 constexpr uint32_t kKSlot = 5 * kAtom;
@@ -91,8 +92,8 @@ constexpr uint32_t OFF_P = OFF_V + kVSlots * kVSlot;
 constexpr uint32_t OFF_Q = OFF_P + 2 * kPBytes;
 constexpr uint32_t OFF_RM = OFF_Q + kQSmemAtoms * kQAtom;   // 2 x 128 FP32: the peer's row maxima
 constexpr uint32_t OFF_LX = OFF_RM + 2 * 512;               // 2 x 128 FP32: the peer's row sums
-constexpr uint32_t OFF_SIG = OFF_LX + 2 * 512;             // per V slot, the own 32 tokens' scales
-constexpr uint32_t OFF_BAR = OFF_SIG + kVSlots * 128;
+constexpr uint32_t OFF_SIG = OFF_LX + 2 * 512;             // per softmax warp, the page's own 32 token scales
+constexpr uint32_t OFF_BAR = OFF_SIG + 4 * 128;
 enum : uint32_t {
   B_K_FULL = 0, B_K_EMPTY = 2, B_V_FULL = 4, B_V_EMPTY = 7, B_S_FULL = 10, B_S_FREE = 12, B_P_LOCAL = 14,
   B_P_FULL = 16, B_P_FREE = 18, B_O_DONE = 20, B_Q_READY = 22, B_FINAL = 23, B_RM_FULL = 24, B_LX_FULL = 26,
@@ -185,36 +186,22 @@ template <> struct Dequant<KV_FP8> {
 };
 
 template <> struct Dequant<KV_FP8PT> {
-  // the FP8 items (codes converted exactly); the own tokens' scales go to the V slot's scale array,
-  // zero past the valid tokens, for the softmax to apply in FP32
-  static constexpr int kOwn = Dequant<KV_FP8>::kOwn, kItems = Dequant<KV_FP8>::kItems;
+  // the FP8 items of a per-token-scaled page (codes converted exactly); the token scales are read by
+  // the softmax warps, which apply them in FP32
   static constexpr int kIters = Dequant<KV_FP8>::kIters;
-  struct Raw { Dequant<KV_FP8>::Raw codes; float s[kIters]; };
-  __device__ static Item at(int q, int c) { return Dequant<KV_FP8>::at(q, c); }
+  using Raw = Dequant<KV_FP8>::Raw;
   __device__ static void load(Raw& r, const DecodeArgs& a, int64_t page, int valid, int c, int t) {
     const uint8_t* base = a.kv + page * kPtPageBytes;
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
       const int q = t + kDQ * i;
-      const Item it = at(q, c);
-      if (q < kItems && it.tok < valid) {
-        ldg_nc32(base + it.tok * kLatent + it.dim, r.codes.v[i]);
-        // one scale per own token: loaded by the item that stores it (the per-SM queue of
-        // outstanding loads, not bandwidth, limits this loop)
-        if (q < kOwn && it.dim == 0) r.s[i] = __ldg(reinterpret_cast<const float*>(base + kPtScaleOff) + it.tok);
-      }
+      const Item it = Dequant<KV_FP8>::at(q, c);
+      if (q < Dequant<KV_FP8>::kItems && it.tok < valid) ldg_nc32(base + it.tok * kLatent + it.dim, r.v[i]);
     }
   }
   __device__ static void store(const Raw& r, const DecodeArgs& a, int64_t page, int valid, int c, int t, uint32_t ks,
                                uint32_t vs, uint32_t sg) {
-    Dequant<KV_FP8>::store(r.codes, a, page, valid, c, t, ks, vs, sg);
-#pragma unroll
-    for (int i = 0; i < kIters; ++i) {
-      const int q = t + kDQ * i;
-      if (q >= kOwn) continue;
-      const Item it = at(q, c);
-      if (it.dim == 0) tc::sts_f32(sg + 4 * it.row, it.tok < valid ? r.s[i] : 0.0f);
-    }
+    Dequant<KV_FP8>::store(r, a, page, valid, c, t, ks, vs, sg);
   }
 };
 
@@ -499,7 +486,7 @@ __device__ void role_pv(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_
 template <int KV>
 __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int seg_e, int c, int h,
                              uint32_t tbase, uint32_t pbuf, uint32_t qs, uint32_t rm, uint32_t lx, uint32_t qver,
-                             const float* sig) {
+                             float* sig) {
   const uint32_t peer = c ^ 1u;
   const uint32_t tl = tbase + (static_cast<uint32_t>(h & ~31) << 16);   // this warp's TMEM lane quarter
   auto wait = [&](uint32_t bar, uint32_t parity, bool cluster, int code) -> bool {
@@ -513,6 +500,17 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
   int cur_req = -1, nq = 0;
   float q_scale = a.scale_log2;
   int64_t pg = cur.done() ? 0 : cur.page(a);
+  // per-token-scaled pages: lane i of every softmax warp reads the scale of own token i of the page
+  // after the current one (zero past the valid tokens) and hands it to its warp through shared memory
+  // when that page comes; each scale multiplies its token's logit and probability in FP32 (not the
+  // row sum)
+  float* sgp = sig + 32 * (h >> 5);
+  auto token_scale = [&](const Cursor& cu, int64_t page) -> float {
+    if (KV != KV_FP8PT || cu.done() || !page_ok(a, page)) return 0.0f;
+    const int tok = kHalf * c + (h & 31);
+    return tok < cu.valid() ? __ldg(reinterpret_cast<const float*>(a.kv + page * kPtPageBytes + kPtScaleOff) + tok) : 0.0f;
+  };
+  float sg_lane = token_scale(cur, pg);
   for (int g = 0; !cur.done(); ++g) {
     const Segment seg = cur.seg;
     if (cur.j == 0 && seg.req != cur_req) {
@@ -599,11 +597,12 @@ __device__ void role_softmax(const DecodeArgs& a, const Sync& sy, int seg_b, int
 
     // ---- logits of the own tokens (buffer s; refilled for page g + 2 only after S_FREE(s)) ----
     if (!wait(B_S_FULL + s, (g >> 1) & 1, false, 128)) return;
-    // per-token-scaled pages: the own tokens' scales sit beside V slot g % 3 (written with it; the
-    // slot is refilled only after this page's P.V, which needs this thread's P first). Each scale
-    // multiplies its token's logit and probability in FP32 (not the row sum).
-    const float* sgp = sig + (g % kVSlots) * 32;
-    if (KV == KV_FP8PT && !wait(B_V_FULL + g % kVSlots, (g / kVSlots) & 1, false, 128)) return;
+    if (KV == KV_FP8PT) {
+      __syncwarp();
+      sgp[h & 31] = sg_lane;
+      __syncwarp();
+      sg_lane = token_scale(nx, npg);
+    }
     tc::tc_fence_after();
     uint32_t sr[32];
     tc::tmem_ld32(tl + TM_S + kHalf * s, sr);
@@ -807,7 +806,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 
   if (warp < 4) {
     role_softmax<KV>(a, sy, seg_b, seg_e, c, tid, tbase, base + OFF_P, base + OFF_Q, base + OFF_RM, base + OFF_LX,
-                     base + OFF_QVER, reinterpret_cast<const float*>(sbase + OFF_SIG));
+                     base + OFF_QVER, reinterpret_cast<float*>(sbase + OFF_SIG));
   } else if (warp < kQkWarpOdd) {
     role_dequant<KV>(a, sy, seg_b, seg_e, c, tid - 128, base + OFF_K, base + OFF_V, base + OFF_SIG);
   } else if (warp == kPvWarp) {
