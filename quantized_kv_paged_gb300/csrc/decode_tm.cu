@@ -25,8 +25,10 @@
 //     scaled by a power of two folded into the head's logit scale); per page read the thread's logits,
 //     update the per-head running maxima lazily (only when a logit passes the maximum by more than 2^8,
 //     base 2; the decision is taken jointly by the four warps), rescale O^T and the row sums then,
-//     write the thread's words of P; at a segment's end sum the row sums over the 64 tokens and
-//     write O / l (or the normalised partial and its log2-sum-exp) from TMEM, one output dim per lane.
+//     write the thread's words of P (up to 32 heads computed against the current maxima before the
+//     joint decision and kept unless it renews them; from 48 heads after it); at a segment's end sum
+//     the row sums over the 64 tokens and write O / l (or the normalised partial and its
+//     log2-sum-exp) from TMEM, one output dim per lane.
 //   warps 4-11 (dequant): raw page bytes from global memory (32-byte loads, the next page's in flight
 //     while the current one is written) into one of two FP16 tile slots; rows past the page's valid
 //     tokens are written as zeros.
