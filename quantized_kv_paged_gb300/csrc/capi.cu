@@ -19,9 +19,11 @@ namespace {
 constexpr uint64_t kAlign = kTableAlign;
 constexpr int kTcSegmentCost = 14;  // pages of work one request start costs the tcgen05 kernel
 // ... and the token-major tcgen05 kernel (its pipeline drains at a request's Q load and segment end;
-// measured on the 64-request mixed batch at 16 / 32 / 64 heads: no charge 119 / 163 / 265 us, 8 pages
-// 98 / 124 / 206 us, 20 pages 103 / 122 / 183 us)
-constexpr int kTmSegmentCost = 20;
+// measured on the 64-request mixed batch at 16 / 32 / 64 heads, one box: 8 pages 97 / 131 / 206 us,
+// 11 pages 97 / 120 / 185, 14 pages 98 / 121 / 177, 20 pages 102 / 124 / 182, 26 pages 104 / 126 /
+// 186; 44 x 32K at 32 heads 292 / 289 / 287 / 291 / 294 us; with no charge, before the batched Q load
+// and the one-pass softmax, 119 / 163 / 265 us)
+constexpr int kTmSegmentCost = 14;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -87,12 +89,12 @@ bool finite_float(float x) { return std::isfinite(x); }
 // The kernel family AUTO picks, from decode-kernel times measured on one GB300 (44 x 32K FP8 and
 // per-token FP8, 10 x 160K and 1 x 1M NVFP4, the 64-request mixed batch; decode kernel only):
 // - 32 to 64 heads on quantized pools: the token-major tcgen05 kernel. FP8 at 32 / 48 / 64 heads
-//   291 / 390 / 405 us against 311 (mma.sync) / 494 / 495 us (CTA pair); per-token FP8 296 / 459 /
+//   287 / 390 / 405 us against 311 (mma.sync) / 494 / 495 us (CTA pair); per-token FP8 296 / 459 /
 //   474 against 322 / 539 / 542 us (mma.sync); NVFP4 10 x 160K at 32 / 64 heads 350 / 484 against 542
 //   (mma.sync) / 544 us, 1M 236 / 333 against 347 / 361 us; mixed batch at 32 / 48 / 64 heads
-//   124 / 173 / 182 against 123 / 183 / 185 us.
+//   121 / 173 / 177 against 123 / 183 / 185 us.
 // - 16 heads: the mma.sync kernel (FP8 200 against 255 us, NVFP4 279 against 313 us, mixed batch 91
-//   against 101 us).
+//   against 98 us).
 // - More heads (and BF16 pools from 64): the tcgen05 CTA-pair kernel, whose 128 head rows cost the
 //   same at any head count; BF16 pools below 64 heads take mma.sync.
 int auto_algo(int num_heads, int kv_dtype) {

@@ -237,6 +237,28 @@ def test_tcgen05_split_charges_request_starts(lib):
     assert a.num_segments == 70 and a.max_worker_pages == 100 and a.min_worker_pages == 0
 
 
+def test_token_major_split_charges_request_starts(lib):
+    """The token-major plan (one worker per SM) also balances pages plus a fixed cost of 14 pages per
+    request a worker starts: workers are at most one request start apart, and requests that fit a
+    worker whole are not cut."""
+    lens = np.array([32768] * 44, np.int32)
+    ptr = np.concatenate([[0], np.cumsum((lens + 63) // 64)]).astype(np.int32)
+    tm = plan(ptr, lens, heads=32, algo=q.ALGO_TCGEN05_TOKENS, sms=152)
+    eq = plan(ptr, lens, heads=16, algo=q.ALGO_MMA_SYNC, sms=152)
+    assert tm.num_workers == eq.num_workers == 152 and tm.ctas_per_worker == 1
+    assert tm.total_pages == eq.total_pages == 44 * 512
+    assert tm.num_segments <= eq.num_segments
+    assert tm.max_worker_pages - tm.min_worker_pages <= 14
+    # 140 requests of 100 pages over 152 workers: equal quotas of 93 pages cut nearly all of them;
+    # one whole request per worker costs 100 + 14 = 114 < 93 + 2 x 14, so none is cut
+    sl = np.array([6400] * 140, np.int32)
+    sp = np.concatenate([[0], np.cumsum((sl + 63) // 64)]).astype(np.int32)
+    a = plan(sp, sl, heads=32, algo=q.ALGO_TCGEN05_TOKENS, sms=152)
+    b = plan(sp, sl, heads=16, algo=q.ALGO_MMA_SYNC, sms=152)
+    assert b.num_segments == 289 and b.max_worker_pages == 93
+    assert a.num_segments == 140 and a.max_worker_pages == 100 and a.min_worker_pages == 0
+
+
 def test_fp8_qk_algo_plans_fp8_pools_only(lib):
     ptr, lens = np.array([0, 2], np.int32), np.array([100], np.int32)
     for kv in (q.KV_FP8_E4M3, q.KV_FP8_PER_TOKEN):
