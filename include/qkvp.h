@@ -105,7 +105,7 @@ typedef enum {
                               QKVP_E_UNSUPPORTED); one CTA per SM. Same arithmetic and tolerance as
                               the other families. AUTO picks it for quantized pools at 32 to 64 heads,
                               where it measured fastest on GB300 (FP8 44 x 32K at 32 / 64 heads:
-                              291 / 405 us against 311 / 495 us for the other families; NVFP4 1M:
+                              287 / 405 us against 311 / 495 us for the other families; NVFP4 1M:
                               236 / 333 against 347 / 361 us). At 16 heads the mma.sync kernel is
                               faster. */
 } qkvp_algo;
